@@ -1,0 +1,212 @@
+"""Pins for the oracle's per-token group quant (CPU only).
+
+Hand-computed groups and layouts come from text fixtures under
+tests/golden/; the rest are properties that hold for any correct
+implementation: the dequantized codes reproduce the input within half an
+E4M3 step, the largest element maps to +-448 under fp32 scales, UE8M0 scales
+are the smallest power of two >= amax/448, and special cases reduce to
+simpler ones (group = whole row, SiLU(gate) = gate for large gates).
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp8_scaled_gemm_mm_gb300 import synth
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _cases():
+    cases, cur = [], None
+    with open(os.path.join(GOLD, "quant_hand_groups.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            key, *rest = line.split()
+            if key == "case":
+                cur = {"name": rest[0]}
+                cases.append(cur)
+            else:
+                cur[key] = rest
+    return cases
+
+
+def _bits(values, dtype):
+    t = torch.tensor(values, dtype=torch.float32).to(torch.bfloat16 if dtype == 0 else torch.float16)
+    return synth.to_bits(t)
+
+
+@pytest.mark.parametrize("case", _cases(), ids=lambda c: c["name"])
+def test_hand_groups(case):
+    dtype = {"bf16": 0, "fp16": 1}[case["dtype"][0]]
+    group = int(case["group"][0])
+    ue8m0 = bool(int(case["ue8m0"][0]))
+    vals = [float(v) for v in case["values"]]
+    x = np.zeros((1, group), np.uint16)
+    x[0, :len(vals)] = _bits(vals, dtype)
+    q, s, e = oracle.group_quant_canonical(x, dtype, group, False, ue8m0)
+    want = np.zeros(group, np.uint8)
+    want[:len(vals)] = [int(c, 16) for c in case["codes"]]
+    assert np.array_equal(q[0], want), [hex(c) for c in q[0, :len(vals)]]
+    assert s.view(np.uint32)[0, 0] == int(case["scale"][0], 16), hex(s.view(np.uint32)[0, 0])
+    if case["byte"][0] != "-":
+        assert e[0, 0] == int(case["byte"][0])
+
+
+def test_ue8m0_packing_fixture():
+    rows = {"rowmajor": [], "colmajor": []}
+    with open(os.path.join(GOLD, "ue8m0_packing.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                key, *vals = line.split()
+                rows[key].append([int(v, 16) for v in vals])
+    x = np.zeros((2, 768), np.uint16)
+    for g in range(6):
+        x[0, g * 128] = _bits([2.0 ** (g - 3)], 0)[0]
+    for colmajor, key in ((False, "rowmajor"), (True, "colmajor")):
+        _, s = oracle.group_quant(x, 0, 128, oracle.SCALE_UE8M0_PACKED, colmajor)
+        want = np.array(rows[key], np.uint32).view(np.int32)
+        assert s.dtype == np.int32 and np.array_equal(s, want), (key, [[hex(v) for v in r] for r in s.view(np.uint32)])
+
+
+def _check_properties(x_bits, dtype, group, fuse, ue8m0):
+    q, s, e = oracle.group_quant_canonical(x_bits, dtype, group, fuse, ue8m0)
+    M, K = q.shape
+    G = K // group
+    if dtype == 0:
+        xv = oracle.bf16_bits_to_f64(x_bits)
+    else:
+        xv = oracle.fp16_bits_to_f64(x_bits)
+    if fuse:
+        gate, up = xv[:, :K], xv[:, K:]
+        with np.errstate(over="ignore"):
+            v = gate / (1.0 + np.exp(-gate)) * up
+    else:
+        v = xv
+    vg = v.reshape(M, G, group)
+    amax = np.abs(vg).max(axis=2)
+    a = np.maximum(amax, float(np.float32(1e-10)))
+    s64 = s.astype(np.float64)
+    # fp32 rounding of a/448; with SiLU in front, the fp32 SiLU also moves amax by a few ulp
+    rel = 2.0 ** -20 if fuse else 2.0 ** -23
+    if ue8m0:
+        # smallest power of two >= a/448
+        assert np.all(np.log2(s64) == np.round(np.log2(s64)))
+        assert np.all(s64 >= a / 448 * (1 - rel))
+        assert np.all(s64 < 2 * a / 448 * (1 + rel))
+        assert np.array_equal(s64, 2.0 ** (e.astype(np.float64) - 127))
+    else:
+        assert np.all(np.abs(s64 - a / 448) <= a / 448 * rel)
+    deq = oracle.e4m3_decode(q).reshape(M, G, group)
+    scaled = vg / s64[:, :, None]                 # the value the code should represent
+    tol = np.maximum(np.abs(scaled) * 2.0 ** -4, 2.0 ** -10) * (1 + 2.0 ** -20) + np.abs(scaled) * 2.0 ** -20
+    if fuse:
+        tol = tol + np.abs(scaled) * 2.0 ** -20 * 8   # fp32 SiLU rounding
+    err = np.abs(deq - np.clip(scaled, -448, 448))
+    assert np.all(err <= tol), float((err - tol).max())
+    assert np.all(np.abs(deq) <= 448)
+    if not ue8m0 and not fuse:
+        # the absmax element of every non-zero group lands on +-448
+        idx = np.abs(vg).argmax(axis=2)
+        top = np.take_along_axis(deq, idx[:, :, None], axis=2)[:, :, 0]
+        nz = amax >= 1e-10
+        assert np.all(np.abs(top[nz]) == 448.0)
+    return q, s, e
+
+
+@pytest.mark.parametrize("dtype", [0, 1])
+@pytest.mark.parametrize("ue8m0", [False, True])
+@pytest.mark.parametrize("group", [32, 64, 128])
+def test_properties_config5_like(dtype, ue8m0, group):
+    x = synth.quant_input(128, 2048, torch.bfloat16 if dtype == 0 else torch.float16, seed=11)
+    _check_properties(synth.to_bits(x), dtype, group, False, ue8m0)
+
+
+@pytest.mark.parametrize("dtype", [0, 1])
+@pytest.mark.parametrize("ue8m0", [False, True])
+def test_properties_fused(dtype, ue8m0):
+    x = synth.quant_input(64, 2 * 1024, torch.bfloat16 if dtype == 0 else torch.float16, seed=12)
+    _check_properties(synth.to_bits(x), dtype, 128, True, ue8m0)
+
+
+def test_fp16_small_groups_never_saturate():
+    # the PR's failure signature: 4095/4096 codes +-448 for fp16 groups with
+    # amax < 6.8e-3 under UE8M0.  Correct output keeps them in range.
+    x = (synth.normal((32, 4096), 1.0, seed=5) * 1e-3).to(torch.float16)
+    q, s, e = oracle.group_quant_canonical(synth.to_bits(x), 1, 128, False, True)
+    assert np.all(e < 127 - 14)           # multipliers above 65504 were in use
+    # a +-448 code only where the scaled value rounds there (>= 432), i.e. at
+    # most the group's largest elements -- not whole groups
+    v = oracle.fp16_bits_to_f64(synth.to_bits(x)).reshape(32, 32, 128)
+    scaled = np.abs(v) / s.astype(np.float64)[:, :, None]
+    sat = ((q & 0x7F) == 0x7E).reshape(32, 32, 128)
+    assert np.all(scaled[sat] >= 432)
+    assert sat.sum() < 0.01 * sat.size
+
+
+def test_whole_row_group_is_per_row():
+    x = synth.to_bits(synth.normal((16, 512), 1.0, seed=6))
+    q1, s1, _ = oracle.group_quant_canonical(x, 0, 512)
+    q2, s2 = oracle.quantize_rows(x, 0)
+    assert np.array_equal(q1, q2) and np.array_equal(s1[:, 0], s2)
+    # and equals the group quant of each row taken on its own
+    for m in (0, 7, 15):
+        qm, sm, _ = oracle.group_quant_canonical(x[m:m + 1], 0, 512)
+        assert np.array_equal(qm[0], q1[m]) and sm[0, 0] == s1[m, 0]
+
+
+def test_fused_large_gate_is_identity():
+    # SiLU(g) = g / (1 + exp(-g)) and exp(-g) < 2^-25 for g >= 18, so in fp32
+    # SiLU(g) == g; with up = 1 the fused quant equals the plain quant of gate.
+    rng = np.random.default_rng(4)
+    gate = torch.tensor(rng.uniform(18, 300, (8, 256)), dtype=torch.float32)
+    gate[:, ::7] *= 1e-2          # mix in ordinary values too (those must differ)
+    up = torch.ones_like(gate)
+    xf = synth.to_bits(torch.cat([gate, up], 1).to(torch.bfloat16))
+    xg = synth.to_bits(gate.to(torch.bfloat16))
+    qf, sf, _ = oracle.group_quant_canonical(xf, 0, 128, True)
+    qg, sg, _ = oracle.group_quant_canonical(xg, 0, 128, False)
+    big = (gate.to(torch.bfloat16).float().numpy() >= 18)
+    assert np.array_equal(sf, sg)          # every group's absmax is a large gate
+    assert np.array_equal(qf[big], qg[big])
+    assert not np.array_equal(qf[~big], qg[~big])
+    # gate and up halves are not interchangeable
+    xs = synth.to_bits(torch.cat([up, gate], 1).to(torch.bfloat16))
+    qs, _, _ = oracle.group_quant_canonical(xs, 0, 128, True)
+    assert not np.array_equal(qs, qf)
+
+
+def test_fused_zero_up_keeps_sign_of_silu():
+    gate = torch.tensor([[-3.0, 2.0] + [0.0] * 126], dtype=torch.float32)
+    up = torch.zeros_like(gate)
+    x = synth.to_bits(torch.cat([gate, up], 1).to(torch.bfloat16))
+    q, s, _ = oracle.group_quant_canonical(x, 0, 128, True)
+    assert q[0, 0] == 0x80 and q[0, 1] == 0x00       # -0 keeps its sign bit
+    assert s.view(np.uint32)[0, 0] == 0x2A7B5123
+
+
+def test_layouts_agree():
+    x = synth.to_bits(synth.quant_input(10, 1024, seed=8))
+    for fmt in (0, 1, 2):
+        _, rm = oracle.group_quant(x, 0, 128, fmt, False)
+        _, cm = oracle.group_quant(x, 0, 128, fmt, True)
+        assert cm.shape[1] == 12 and np.all(cm[:, 10:] == 0)
+        assert np.array_equal(cm[:, :10].T, rm)
+
+
+def test_scatter_rows_equal_plain_rows():
+    x = synth.to_bits(synth.quant_input(40, 512, seed=9))
+    dst, R = synth.routing(40, topk=8, num_experts=16, align=8)
+    assert len(np.unique(dst)) == dst.size and dst.min() >= 0 and dst.max() < R
+    q, s = oracle.group_quant(x, 0, 128, oracle.SCALE_UE8M0_PACKED, True)
+    qd, sd = oracle.group_quant_scatter(x, 0, 128, dst, R)
+    for m in range(40):
+        for d in dst[m]:
+            assert np.array_equal(qd[d], q[m]) and np.array_equal(sd[:, d], s[:, m])
+    untouched = np.setdiff1d(np.arange(R), dst.ravel())
+    assert np.all(qd[untouched] == 0) and np.all(sd[:, untouched] == 0)
