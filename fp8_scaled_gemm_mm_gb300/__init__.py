@@ -1,0 +1,183 @@
+"""Python binding of libfp8mm, the GB300 (sm_103a) FP8 linear-layer hot path.
+
+Thin marshalling over the C ABI declared in ``include/fp8mm.h``: every function
+here passes device pointers, sizes and the current CUDA stream to the library
+and raises ``Fp8mmError`` on a non-zero status.  All arithmetic happens in the
+library's CUDA kernels; there is no other implementation to fall back to, and
+importing this module fails loudly if the library has not been built.
+
+Operations (see the header for full semantics):
+  per_token_group_quant_fp8          bf16/fp16 -> E4M3FN codes + scales
+  per_token_group_quant_fp8_scatter  the same, written to topk destination rows
+  fp8_scaled_mm                      out = round(a_s * b_s * A B^T (+ bias))
+"""
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "Fp8mmError", "lib", "per_token_group_quant_fp8", "per_token_group_quant_fp8_scatter",
+    "fp8_scaled_mm", "get_device_status", "selftest_bounded_wait", "scale_shape", "scale_dtype",
+    "alloc_group_quant_outputs", "SCALE_FP32", "SCALE_FP32_POW2", "SCALE_UE8M0_PACKED",
+    "A_TENSOR", "A_ROW", "A_GROUP128", "A_GROUP128_COLMAJOR", "B_TENSOR", "B_COL",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libfp8mm.so")
+
+# status codes
+OK, EINVAL, EALIGN, EUNSUPPORTED, ECUDA, ETIMEOUT = 0, -1, -2, -3, -4, -5
+# scale formats of the group quant
+SCALE_FP32, SCALE_FP32_POW2, SCALE_UE8M0_PACKED = 0, 1, 2
+# GEMM scale modes
+A_TENSOR, A_ROW, A_GROUP128, A_GROUP128_COLMAJOR = 0x0, 0x1, 0x2, 0x3
+B_TENSOR, B_COL = 0x00, 0x10
+
+_DTYPE_CODE = {torch.bfloat16: 0, torch.float16: 1}
+
+
+class Fp8mmError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {lib().fp8mm_status_string(status).decode()} ({status})")
+
+
+_LIB = None
+
+
+def lib():
+    """The loaded libfp8mm (raises if it has not been built)."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"libfp8mm is not built ({LIB_PATH} missing); run __graft_entry__.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I, I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+        L.fp8_scaled_mm.argtypes = [P, P, P, P, I, P, P, I, I64, I64, I64, I64, I64, I, P]
+        L.fp8_scaled_mm.restype = I
+        L.per_token_group_quant_fp8.argtypes = [P, I, P, P, I64, I64, I, I, I, I, P]
+        L.per_token_group_quant_fp8.restype = I
+        L.per_token_group_quant_fp8_scatter.argtypes = [P, I, P, I, I64, P, P, I64, I64, I, I, I, P]
+        L.per_token_group_quant_fp8_scatter.restype = I
+        L.fp8mm_get_device_status.argtypes = [I, I]
+        L.fp8mm_get_device_status.restype = I
+        L.fp8mm_selftest_bounded_wait.argtypes = [I64, P]
+        L.fp8mm_selftest_bounded_wait.restype = I
+        L.fp8mm_status_string.argtypes = [I]
+        L.fp8mm_status_string.restype = ctypes.c_char_p
+        L.fp8mm_version.restype = I
+        _LIB = L
+    return _LIB
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _check(status: int, what: str):
+    if status != OK:
+        raise Fp8mmError(status, what)
+
+
+# ----------------------------------------------------------- group quant
+
+def scale_shape(rows: int, K: int, group: int, fmt: int, colmajor: bool):
+    """Shape of the scale tensor the kernels write (see include/fp8mm.h)."""
+    G = K // group
+    W = (G + 3) // 4
+    pad = (rows + 3) // 4 * 4
+    if fmt == SCALE_UE8M0_PACKED:
+        return (W, pad) if colmajor else (rows, W)
+    return (G, pad) if colmajor else (rows, G)
+
+
+def scale_dtype(fmt: int):
+    return torch.int32 if fmt == SCALE_UE8M0_PACKED else torch.float32
+
+
+def alloc_group_quant_outputs(rows: int, K: int, group: int, fmt: int = SCALE_FP32, colmajor: bool = False,
+                              device="cuda", zero: bool = False):
+    """Allocate codes [rows, K] uint8 and the scale tensor for these flags."""
+    mk = torch.zeros if zero else torch.empty
+    q = mk((rows, K), dtype=torch.uint8, device=device)
+    s = mk(scale_shape(rows, K, group, fmt, colmajor), dtype=scale_dtype(fmt), device=device)
+    return q, s
+
+
+def per_token_group_quant_fp8(x, q, s, group: int, ue8m0: int = SCALE_FP32, scale_colmajor: bool = False,
+                              fuse_silu_mul: bool = False, stream=None, x_dtype=None, M=None, K=None):
+    """Quantize x [M, K] (or [M, 2K] with fuse_silu_mul) into q [M, K] and s."""
+    if x_dtype is None:
+        x_dtype = _DTYPE_CODE[x.dtype]
+    if M is None:
+        M = x.shape[0]
+    if K is None:
+        K = x.shape[1] // 2 if fuse_silu_mul else x.shape[1]
+    st = lib().per_token_group_quant_fp8(_ptr(x), x_dtype, _ptr(q), _ptr(s), M, K, group, int(ue8m0),
+                                         int(bool(scale_colmajor)), int(bool(fuse_silu_mul)), _stream(stream))
+    _check(st, "per_token_group_quant_fp8")
+
+
+def per_token_group_quant_fp8_scatter(x, dst_row, q, s, group: int, ue8m0: int = SCALE_UE8M0_PACKED,
+                                      scale_colmajor: bool = True, stream=None, x_dtype=None, M=None, K=None,
+                                      topk=None, num_dst_rows=None):
+    """Quantize x [M, K] once per token and write it to rows dst_row[m, :] of q / s."""
+    if x_dtype is None:
+        x_dtype = _DTYPE_CODE[x.dtype]
+    if M is None:
+        M, K = x.shape
+    if topk is None:
+        topk = dst_row.shape[1]
+    if num_dst_rows is None:
+        num_dst_rows = q.shape[0]
+    st = lib().per_token_group_quant_fp8_scatter(_ptr(x), x_dtype, _ptr(dst_row), topk, num_dst_rows, _ptr(q),
+                                                 _ptr(s), M, K, group, int(ue8m0), int(bool(scale_colmajor)),
+                                                 _stream(stream))
+    _check(st, "per_token_group_quant_fp8_scatter")
+
+
+# ------------------------------------------------------------------ GEMM
+
+def fp8_scaled_mm(A, B, a_scale, b_scale, scale_mode: int, out, bias=None, deterministic: bool = False,
+                  stream=None, M=None, N=None, K=None, lda=None, ldb=None):
+    """out [M, N] (bf16 / fp16) = round(a_s * b_s * A[:, :K] B[:, :K]^T (+ bias)).
+
+    A: uint8 / float8_e4m3fn [M, lda], B: [N, ldb] (row strides in elements).
+    """
+    if M is None:
+        M = A.shape[0]
+    if N is None:
+        N = B.shape[0]
+    if K is None:
+        K = A.shape[1]
+    if lda is None:
+        lda = A.stride(0) if A.dim() == 2 else K
+    if ldb is None:
+        ldb = B.stride(0) if B.dim() == 2 else K
+    out_dtype = _DTYPE_CODE[out.dtype] if isinstance(out, torch.Tensor) else 0
+    st = lib().fp8_scaled_mm(_ptr(A), _ptr(B), _ptr(a_scale), _ptr(b_scale), int(scale_mode), _ptr(bias),
+                             _ptr(out), out_dtype, M, N, K, lda, ldb, int(bool(deterministic)), _stream(stream))
+    _check(st, "fp8_scaled_mm")
+
+
+# ------------------------------------------------------------ diagnostics
+
+def get_device_status(device: int = -1, clear: bool = True) -> int:
+    return lib().fp8mm_get_device_status(device, int(clear))
+
+
+def selftest_bounded_wait(timeout_ns: int, stream=None):
+    _check(lib().fp8mm_selftest_bounded_wait(int(timeout_ns), _stream(stream)), "fp8mm_selftest_bounded_wait")

@@ -1,0 +1,503 @@
+// gemm.cu -- E4M3 x E4M3 scaled GEMM on sm_103a tensor cores (tcgen05 + TMEM + TMA).
+//
+// Computes out[m,n] = round(a_s * b_s * sum_k A[m,k] B[n,k] (+ bias[n])), the rowwise /
+// per-tensor scaled FP8 GEMM of sglang PR #34318 ("[Kernel] Route large SM90
+// row/column-scaled FP8 GEMMs to Torch", Summary) and of the prhub summary of
+// sglang PR #33148 (per-tensor scalar scales used as they are, weight [N,K] K-major).
+//
+// One persistent CTA per SM (192 threads), warp-specialized:
+//   warp 0      TMA producer: A [128 x 128] and B [BN x 128] byte tiles, 128-byte
+//               swizzle, into a STAGES-deep shared-memory ring (full/empty mbarriers).
+//               Out-of-bounds rows and the K tail arrive as zeros.
+//   warp 1      allocates TMEM and issues tcgen05.mma (M=128, N=BN, K=32 per
+//               instruction, fp32 accumulate) from one thread; tcgen05.commit frees
+//               each stage and publishes each finished accumulator.
+//   warps 2..5  epilogue: tcgen05.ld 32 columns at a time, scale (and bias), round to
+//               bf16/fp16, stage in swizzled shared memory, TMA store (edges clipped).
+// Two TMEM accumulators alternate so that the epilogue of tile i overlaps the
+// mainloop of tile i+1.  Tiles are visited in groups of `raster` M-blocks so that
+// the CTAs running at the same time share A and B panels in L2.
+//
+// Per-group A scales (one per 128-wide K block, the layout the group quant produces):
+// every K block goes to its own TMEM accumulator and the epilogue promotes it,
+// acc += a_s[m, kb] * partial_kb, in fp32 registers.
+//
+// Deterministic mode uses one tile shape (BM=128, BN=64, BK=128), one instruction
+// shape and the natural K-block order for every problem, with no split of K, so row
+// m of the result does not depend on M or on the other rows (sglang PR #44861,
+// Modifications: fixed N=64/K=128 reduction tiles, zero-filled K tails).
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace fp8mm {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 128;           // K elements (= bytes) per stage: one 128-byte swizzle row
+constexpr int UMMA_K = 32;        // K per tcgen05.mma for 8-bit operands
+constexpr int kEpiWarps = 4;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
+
+struct GemmArgs {
+  int M, N, K;
+  int num_kb;
+  int m_blocks, n_blocks, tiles;
+  int raster;
+  int a_mode, b_mode;
+  int64_t a_ld;
+  const float* a_scale;
+  const float* b_scale;
+  const __nv_bfloat16* bias;
+  int out_fp16;
+  int* status;
+  uint64_t timeout_ns;
+};
+
+__host__ __device__ constexpr uint32_t pow2_at_least(uint32_t v) {
+  uint32_t r = 32;
+  while (r < v) r <<= 1;
+  return r;
+}
+
+template <int BN, int STAGES>
+struct Layout {
+  static constexpr int A_BYTES = BM * BK;
+  static constexpr int B_BYTES = BN * BK;
+  static constexpr int D_BYTES = 32 * 64;  // one epilogue warp's staging buffer: 32 rows x 64 bytes
+  static constexpr int OFF_A = 0;
+  static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+  static constexpr int OFF_D = OFF_B + STAGES * B_BYTES;
+  static constexpr int OFF_BAR = OFF_D + kEpiWarps * 2 * D_BYTES;
+  static constexpr int NBARS = 2 * STAGES + 5;
+  static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
+  static constexpr int BYTES = OFF_MISC + 16;
+  static constexpr int ALLOC = BYTES + 1024;  // slack to align the base to 1024
+  static constexpr uint32_t TMEM_COLS = pow2_at_least(2 * BN);
+  static_assert(B_BYTES % 1024 == 0, "B stage must keep 1024-byte alignment");
+  static_assert(ALLOC <= 232448, "shared memory budget");
+};
+
+__device__ __forceinline__ void tile_coords(const GemmArgs& p, int t, int& mb, int& nb) {
+  const int per_group = p.raster * p.n_blocks;
+  const int g = t / per_group;
+  const int first = g * p.raster;
+  const int gsz = min(p.m_blocks - first, p.raster);
+  const int r = t - g * per_group;
+  mb = first + r % gsz;
+  nb = r / gsz;
+}
+
+__device__ __forceinline__ float a_scale_at(const GemmArgs& p, int row, int kb) {
+  if (row >= p.M) return 0.0f;
+  switch (p.a_mode) {
+    case FP8MM_SCALE_A_TENSOR: return __ldg(p.a_scale);
+    case FP8MM_SCALE_A_ROW: return __ldg(p.a_scale + row);
+    case FP8MM_SCALE_A_GROUP128: return __ldg(p.a_scale + static_cast<int64_t>(row) * p.a_ld + kb);
+    default: return __ldg(p.a_scale + static_cast<int64_t>(kb) * p.a_ld + row);
+  }
+}
+
+// b_scale and bias for the 32 columns n0..n0+31 (zeros beyond N).
+__device__ __forceinline__ void load_col_vectors(const GemmArgs& p, int n0, float (&sb)[32], float (&bs)[32]) {
+  if (p.b_mode == 0) {
+    const float s = __ldg(p.b_scale);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) sb[j] = s;
+  } else if ((reinterpret_cast<uintptr_t>(p.b_scale) & 15u) == 0) {
+#pragma unroll
+    for (int v = 0; v < 8; ++v) {
+      float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (n0 + 4 * v < p.N) f = __ldg(reinterpret_cast<const float4*>(p.b_scale + n0) + v);
+      sb[4 * v] = f.x;
+      sb[4 * v + 1] = f.y;
+      sb[4 * v + 2] = f.z;
+      sb[4 * v + 3] = f.w;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) sb[j] = (n0 + j < p.N) ? __ldg(p.b_scale + n0 + j) : 0.0f;
+  }
+  if (p.bias == nullptr) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) bs[j] = 0.0f;
+  } else if ((reinterpret_cast<uintptr_t>(p.bias) & 15u) == 0) {
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      uint4 u = make_uint4(0, 0, 0, 0);
+      if (n0 + 8 * v < p.N) u = __ldg(reinterpret_cast<const uint4*>(p.bias + n0) + v);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        bs[8 * v + 2 * i] = __uint_as_float(w[i] << 16);
+        bs[8 * v + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) bs[j] = (n0 + j < p.N) ? __bfloat162float(p.bias[n0 + j]) : 0.0f;
+  }
+}
+
+__device__ __forceinline__ uint32_t pack2(float a, float b, int fp16) {
+  if (fp16) {
+    const __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  }
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Write one warp's 32 x 32 output block (this lane = one row) into its staging buffer
+// (64-byte swizzle) and TMA-store it at column n0, row r0.  Blocks that lie wholly
+// outside the output are skipped; partial ones are clipped by the TMA unit.
+// Returns whether a store was issued (the caller then switches staging buffers).
+__device__ __forceinline__ bool store_block(const CUtensorMap* tmD, uint8_t* buf, const uint32_t (&w)[16],
+                                            int lane, int n0, int r0, int M, int N) {
+  if (r0 >= M || n0 >= N) return false;
+  if (lane == 0) bulk_wait_read<1>();  // the store issued from this buffer two blocks ago has read it
+  __syncwarp();
+  uint8_t* row = buf + lane * 64;
+  const int sw = (lane >> 1) & 3;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    *reinterpret_cast<uint4*>(row + ((j ^ sw) << 4)) = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(tmD, buf, n0, r0);
+    bulk_commit();
+  }
+  return true;
+}
+
+template <int BN, int STAGES, bool GROUP_A>
+__global__ void __launch_bounds__(kThreads, 1)
+    fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmD, const GemmArgs p) {
+  using L = Layout<BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  // 128-byte swizzle atoms and the UMMA descriptors need 1024-byte aligned shared addresses
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmD);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], kEpiWarps);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, L::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------- producer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      int64_t issued = 0;
+      for (int t = blockIdx.x; t < p.tiles && !*abort_flag; t += gridDim.x) {
+        int mb, nb;
+        tile_coords(p, t, mb, nb);
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status, p.timeout_ns)) break;
+          mbar_arrive_expect_tx(&full[stage], L::A_BYTES + L::B_BYTES);
+          tma_load_2d(&tmA, &full[stage], smem + L::OFF_A + stage * L::A_BYTES, kb * BK, mb * BM);
+          tma_load_2d(&tmB, &full[stage], smem + L::OFF_B + stage * L::B_BYTES, kb * BK, nb * BN);
+          ++issued;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Every load this CTA issued must have landed before the CTA may exit.
+      const int outstanding = static_cast<int>(issued < STAGES ? issued : STAGES);
+      for (int j = 1; j <= outstanding; ++j) {
+        int s = static_cast<int>(stage) - j;
+        uint32_t ph = phase;
+        if (s < 0) {
+          s += STAGES;
+          ph ^= 1u;
+        }
+        volatile int never = 0;
+        mbar_wait(&full[s], ph, &never, p.status, p.timeout_ns);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issue
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
+      uint32_t stage = 0, phase = 0, acc_i = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < p.tiles; t += gridDim.x) {
+        for (int kb = 0; ok && kb < p.num_kb; ++kb) {
+          const uint32_t acc = acc_i & 1u;
+          if (GROUP_A || kb == 0) {
+            ok = mbar_wait(&tempty[acc], ((acc_i >> 1) & 1u) ^ 1u, abort_flag, p.status, p.timeout_ns);
+            if (!ok) break;
+            tc_fence_after();
+          }
+          ok = mbar_wait(&full[stage], phase, abort_flag, p.status, p.timeout_ns);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t d = tmem_base + acc * BN;
+          const uint64_t adesc = smem_desc_sw128(smem_u32(smem + L::OFF_A + stage * L::A_BYTES));
+          const uint64_t bdesc = smem_desc_sw128(smem_u32(smem + L::OFF_B + stage * L::B_BYTES));
+#pragma unroll
+          for (int k = 0; k < BK / UMMA_K; ++k) {
+            const uint32_t accumulate = (GROUP_A ? k : (kb | k)) != 0 ? 1u : 0u;
+            mma_f8f6f4(d, adesc + static_cast<uint64_t>(k * UMMA_K / 16),
+                       bdesc + static_cast<uint64_t>(k * UMMA_K / 16), idesc, accumulate);
+          }
+          mma_commit(&empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          if (GROUP_A || kb == p.num_kb - 1) {
+            mma_commit(&tfull[acc]);
+            ++acc_i;
+          }
+        }
+      }
+      // All MMAs issued here must be complete before TMEM is released.
+      mma_commit(drain);
+      volatile int never = 0;
+      mbar_wait(drain, 0, &never, p.status, p.timeout_ns);
+    }
+  } else {
+    // ------------------------------------------------------------- epilogue
+    const int ew = warp - 2;                  // staging buffer owner
+    const int q = warp & 3;                   // TMEM lane quarter this warp may access
+    uint8_t* stage_buf = smem + L::OFF_D + ew * 2 * L::D_BYTES;
+    int dbuf = 0;
+    uint32_t acc_i = 0;
+    const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    for (int t = blockIdx.x; t < p.tiles; t += gridDim.x) {
+      int mb, nb;
+      tile_coords(p, t, mb, nb);
+      const int row = mb * BM + q * 32 + lane;
+      const int r0 = mb * BM + q * 32;
+      const int nbase = nb * BN;
+      if constexpr (!GROUP_A) {
+        const uint32_t acc = acc_i & 1u;
+        if (!mbar_wait(&tfull[acc], (acc_i >> 1) & 1u, abort_flag, p.status, p.timeout_ns)) break;
+        tc_fence_after();
+        const float sa = a_scale_at(p, row, 0);
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(lane_addr + acc * BN + c * 32, r);
+          tmem_ld_wait();
+          if (c == BN / 32 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[acc]);
+          }
+          float sb[32], bs[32];
+          load_col_vectors(p, nbase + c * 32, sb, bs);
+          uint32_t w[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float v0 = __uint_as_float(r[2 * j]) * sa * sb[2 * j] + bs[2 * j];
+            const float v1 = __uint_as_float(r[2 * j + 1]) * sa * sb[2 * j + 1] + bs[2 * j + 1];
+            w[j] = pack2(v0, v1, p.out_fp16);
+          }
+          if (store_block(&tmD, stage_buf + dbuf * L::D_BYTES, w, lane, nbase + c * 32, r0, p.M, p.N)) dbuf ^= 1;
+        }
+        ++acc_i;
+      } else {
+        float accum[BN];
+#pragma unroll
+        for (int j = 0; j < BN; ++j) accum[j] = 0.0f;
+        bool ok = true;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          const uint32_t acc = acc_i & 1u;
+          ok = mbar_wait(&tfull[acc], (acc_i >> 1) & 1u, abort_flag, p.status, p.timeout_ns);
+          if (!ok) break;
+          tc_fence_after();
+          const float sa = a_scale_at(p, row, kb);
+#pragma unroll
+          for (int c = 0; c < BN / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(lane_addr + acc * BN + c * 32, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) accum[c * 32 + j] = fmaf(sa, __uint_as_float(r[j]), accum[c * 32 + j]);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tempty[acc]);
+          ++acc_i;
+        }
+        if (!ok) break;
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) {
+          float sb[32], bs[32];
+          load_col_vectors(p, nbase + c * 32, sb, bs);
+          uint32_t w[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float v0 = accum[c * 32 + 2 * j] * sb[2 * j] + bs[2 * j];
+            const float v1 = accum[c * 32 + 2 * j + 1] * sb[2 * j + 1] + bs[2 * j + 1];
+            w[j] = pack2(v0, v1, p.out_fp16);
+          }
+          if (store_block(&tmD, stage_buf + dbuf * L::D_BYTES, w, lane, nbase + c * 32, r0, p.M, p.N)) dbuf ^= 1;
+        }
+      }
+    }
+    if (lane == 0) bulk_wait<0>();
+    __syncwarp();
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, L::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
+struct Config {
+  int bn, stages;
+  bool group_a;
+};
+
+template <int BN, int STAGES, bool GROUP_A>
+cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td, const GemmArgs& p,
+                   int grid, cudaStream_t st) {
+  using L = Layout<BN, STAGES>;
+  auto kern = fp8_gemm_kernel<BN, STAGES, GROUP_A>;
+  static int configured_dev = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_dev != dev) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
+    if (e != cudaSuccess) return e;
+    configured_dev = dev;
+  }
+  kern<<<grid, kThreads, L::ALLOC, st>>>(ta, tb, td, p);
+  return cudaGetLastError();
+}
+
+int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
+
+// Shape-keyed tile table.  Deterministic mode always takes the same row.
+Config pick_config(int64_t M, int64_t N, bool deterministic, bool group_a, int sms) {
+  if (group_a) return {64, 8, true};
+  if (deterministic) return {64, 8, false};
+  const int mblk = ceil_div(M, BM);
+  if (static_cast<int64_t>(mblk) * ceil_div(N, 256) >= sms) return {256, 4, false};
+  if (static_cast<int64_t>(mblk) * ceil_div(N, 128) >= sms) return {128, 6, false};
+  return {64, 8, false};
+}
+
+}  // namespace
+}  // namespace fp8mm
+
+using namespace fp8mm;
+
+extern "C" int fp8_scaled_mm(const void* A, const void* B, const float* a_scale, const float* b_scale, int scale_mode,
+                             const void* bias, void* out, int out_dtype, int64_t M, int64_t N, int64_t K, int64_t lda,
+                             int64_t ldb, int deterministic, fp8mm_stream_t stream) {
+  const int a_mode = scale_mode & 0xF;
+  const int b_mode = (scale_mode >> 4) & 0xF;
+  if (M < 0 || N < 0) return FP8MM_EINVAL;
+  if (a_mode > FP8MM_SCALE_A_GROUP128_COLMAJOR || b_mode > 1 || (scale_mode & ~0xFF)) return FP8MM_EINVAL;
+  if (out_dtype != FP8MM_DTYPE_BF16 && out_dtype != FP8MM_DTYPE_FP16) return FP8MM_EINVAL;
+  if (M > 0x7fffffff || N > 0x7fffffff || K > 0x7fffffff) return FP8MM_EINVAL;
+  if (K <= 0 || K % 16 != 0 || lda < K || ldb < K) return FP8MM_EINVAL;
+  if (lda % 16 != 0 || ldb % 16 != 0 || N % 8 != 0) return FP8MM_EALIGN;
+  const bool group_a = a_mode >= FP8MM_SCALE_A_GROUP128;
+  if (group_a && K % 128 != 0) return FP8MM_EINVAL;
+  if (M == 0 || N == 0) return FP8MM_OK;
+  if (!A || !B || !a_scale || !b_scale || !out) return FP8MM_EINVAL;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(out)) return FP8MM_EALIGN;
+  if ((reinterpret_cast<uintptr_t>(a_scale) & 3u) || (reinterpret_cast<uintptr_t>(b_scale) & 3u) ||
+      (reinterpret_cast<uintptr_t>(bias) & 1u))
+    return FP8MM_EALIGN;
+  {
+    // out must not overlap the inputs
+    const uintptr_t o0 = reinterpret_cast<uintptr_t>(out), o1 = o0 + static_cast<uintptr_t>(M * N * 2);
+    auto overlaps = [&](const void* p, int64_t bytes) {
+      const uintptr_t b0 = reinterpret_cast<uintptr_t>(p);
+      return p && b0 < o1 && o0 < b0 + static_cast<uintptr_t>(bytes);
+    };
+    if (overlaps(A, (M - 1) * lda + K) || overlaps(B, (N - 1) * ldb + K) || overlaps(bias, N * 2))
+      return FP8MM_EINVAL;
+  }
+  int* status = status_word_device_ptr();
+  const int sms = num_sms();
+  if (!status || sms <= 0) return FP8MM_ECUDA;
+
+  const Config cfg = pick_config(M, N, deterministic != 0, group_a, sms);
+  CUtensorMap ta, tb, td;
+  if (!make_tma_2d(&ta, const_cast<void*>(A), CU_TENSOR_MAP_DATA_TYPE_UINT8, K, M, lda, BK, BM,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tma_2d(&tb, const_cast<void*>(B), CU_TENSOR_MAP_DATA_TYPE_UINT8, K, N, ldb, BK, cfg.bn,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tma_2d(&td, out, out_dtype == FP8MM_DTYPE_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                           : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                   N, M, N * 2, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+    return FP8MM_ECUDA;
+
+  GemmArgs p;
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.num_kb = ceil_div(K, BK);
+  p.m_blocks = ceil_div(M, BM);
+  p.n_blocks = ceil_div(N, cfg.bn);
+  p.tiles = p.m_blocks * p.n_blocks;
+  p.raster = 16;
+  p.a_mode = a_mode;
+  p.b_mode = b_mode;
+  p.a_ld = a_mode == FP8MM_SCALE_A_GROUP128 ? K / 128 : (M + 3) / 4 * 4;
+  p.a_scale = a_scale;
+  p.b_scale = b_scale;
+  p.bias = static_cast<const __nv_bfloat16*>(bias);
+  p.out_fp16 = out_dtype == FP8MM_DTYPE_FP16;
+  p.status = status;
+  p.timeout_ns = kWaitTimeoutNs;
+  const int grid = p.tiles < sms ? p.tiles : sms;
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (cfg.group_a)
+    e = launch<64, 8, true>(ta, tb, td, p, grid, st);
+  else if (cfg.bn == 256)
+    e = launch<256, 4, false>(ta, tb, td, p, grid, st);
+  else if (cfg.bn == 128)
+    e = launch<128, 6, false>(ta, tb, td, p, grid, st);
+  else
+    e = launch<64, 8, false>(ta, tb, td, p, grid, st);
+  return e == cudaSuccess ? FP8MM_OK : FP8MM_ECUDA;
+}

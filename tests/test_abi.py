@@ -1,0 +1,95 @@
+"""The C-ABI library builds, loads and exports every symbol its header
+declares; host-side validation rejects bad arguments before any CUDA call
+(CPU only: nothing here launches a kernel)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = []
+    inc = os.path.join(ROOT, "include")
+    for fn in sorted(os.listdir(inc)):
+        if fn.endswith(".h"):
+            text = open(os.path.join(inc, fn)).read()
+            names += re.findall(r"FP8MM_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+    return names
+
+
+@pytest.fixture(scope="module")
+def L():
+    from fp8_scaled_gemm_mm_gb300 import build
+    build.build()
+    import fp8_scaled_gemm_mm_gb300 as fm
+    return fm.lib()
+
+
+def test_header_declares_the_entry_points():
+    names = set(_declared())
+    for n in ("fp8_scaled_mm", "per_token_group_quant_fp8", "per_token_group_quant_fp8_scatter",
+              "fp8mm_get_device_status", "fp8mm_status_string", "fp8mm_version"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in _declared():
+        assert hasattr(L, name), name
+
+
+def test_status_strings_and_version(L):
+    assert L.fp8mm_version() >> 16 == 1
+    for code in (0, -1, -2, -3, -4, -5):
+        assert L.fp8mm_status_string(code).startswith(b"FP8MM_")
+
+
+def test_quant_argument_validation(L):
+    q = L.per_token_group_quant_fp8
+    fake = 1 << 20   # never dereferenced: validation fails first
+    # K not a multiple of 16, group not dividing K, bad group, bad dtype, bad format
+    assert q(fake, 0, fake, fake, 4, 72, 32, 0, 0, 0, None) == -1
+    assert q(fake, 0, fake, fake, 4, 2048 + 64, 128, 0, 0, 0, None) == -1
+    assert q(fake, 0, fake, fake, 4, 2048, 96, 0, 0, 0, None) == -1
+    assert q(fake, 2, fake, fake, 4, 2048, 128, 0, 0, 0, None) == -1
+    assert q(fake, 0, fake, fake, 4, 2048, 128, 3, 0, 0, None) == -1
+    assert q(fake, 0, fake, fake, -1, 2048, 128, 0, 0, 0, None) == -1
+    # empty batch: nothing to do, nothing launched
+    assert q(None, 0, None, None, 0, 2048, 128, 0, 0, 0, None) == 0
+    # null pointers with work to do
+    assert q(None, 0, fake, fake, 4, 2048, 128, 0, 0, 0, None) == -1
+    # misaligned input / codes
+    assert q(fake + 2, 0, fake, fake, 4, 2048, 128, 0, 0, 0, None) == -2
+    assert q(fake, 0, fake + 8, fake, 4, 2048, 128, 0, 0, 0, None) == -2
+    s = L.per_token_group_quant_fp8_scatter
+    assert s(fake, 0, None, 8, 64, fake, fake, 4, 2048, 128, 2, 1, None) == -1
+    assert s(fake, 0, fake, 0, 64, fake, fake, 4, 2048, 128, 2, 1, None) == -1
+
+
+def test_gemm_argument_validation(L):
+    g = L.fp8_scaled_mm
+    f = 1 << 20
+    ok_args = dict(A=f, B=f + (1 << 24), a=f + (2 << 24), b=f + (3 << 24), mode=0x11, bias=None, out=f + (4 << 24),
+                   od=0, M=64, N=256, K=512, lda=512, ldb=512, det=0)
+
+    def call(**kw):
+        a = dict(ok_args, **kw)
+        return g(a["A"], a["B"], a["a"], a["b"], a["mode"], a["bias"], a["out"], a["od"], a["M"], a["N"], a["K"],
+                 a["lda"], a["ldb"], a["det"], None)
+
+    assert call(K=72, lda=80, ldb=80) == -1           # K % 16
+    assert call(K=0) == -1                            # empty reduction
+    assert call(lda=256) == -1                        # lda < K
+    assert call(lda=520) == -2                        # lda % 16
+    assert call(N=260) == -2                          # N % 8
+    assert call(mode=0x4) == -1                       # bad A mode
+    assert call(mode=0x21) == -1                      # bad B mode
+    assert call(od=2) == -1                           # bad out dtype
+    assert call(mode=0x12, K=80, lda=80, ldb=80) == -1  # group scales need K % 128
+    assert call(A=f + 8) == -2                        # misaligned A
+    assert call(out=f + 4) == -2                      # misaligned out
+    assert call(out=f + 16) == -1                     # out overlaps A
+    assert call(M=0) == 0                             # empty: no launch
+    assert call(A=None) == -1
