@@ -1,0 +1,450 @@
+#!/usr/bin/env python3
+"""Benchmark of the FP8 linear hot path on GB300.
+
+One step = the five large rowwise-scaled prefill GEMMs of the pages' kernel
+table (sglang PR #34318, "Kernel results": M x K x N = 8320x5376x21504,
+8320x5376x14336, 23216x5376x28672, 15760x5376x28672, 8320x14336x5376), each
+preceded by the per-token quantization of its bf16 activation (group = K, fp32
+row scales) that produces the GEMM's A operand:
+
+    X bf16 [M,K] --per_token_group_quant_fp8--> A e4m3 [M,K], a_s [M]
+    A, B e4m3 [N,K], a_s, b_s [N] --fp8_scaled_mm--> D bf16 [M,N]
+
+Weights are ~N(0, 0.02) bf16 quantized per output channel once at set-up (by
+the same quant kernel), activations ~N(0, 1); inputs stay resident in HBM.
+value = sum 2MNK over the step / step time (TFLOP/s), aggregated over ranks.
+
+Also reported: the group-128 quant kernel alone on its largest workload
+(M=8192, K=7168 bf16, UE8M0 packed column-major scales, plain and fused
+SiLU*up) in GB/s; the roofline of the dominant kernel (the GEMM); the
+end-to-end figure through the C ABI with host buffers; the oracle timed on
+the host cores on a bounded sample (cpu_baseline); SM clocks sampled during
+the timed region.
+
+--impl reference times the CPU oracle (the only reference implementation of
+this path) on a bounded sample of the same workload.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "FP8 scaled-GEMM TFLOP/s & % of FP8 peak; group-quant GB/s & % of HBM peak"
+SHAPES = [(8320, 5376, 21504), (8320, 5376, 14336), (23216, 5376, 28672), (15760, 5376, 28672),
+          (8320, 14336, 5376)]  # (M, K, N)
+# torch._scaled_mm on H100 80GB for the same five shapes (pages' kernel table): sum 2MNK / sum time
+H100_TORCH_US = [1351.1, 896.4, 5295.9, 3570.9, 843.9]
+QUANT_M, QUANT_K = 8192, 7168
+FP8_OVER_BF16 = 2.0      # nominal dense FP8 : BF16 tensor rate on GB300 (4.5 : 2.25 PFLOP/s)
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
+L2_FLUSH_BYTES = 512 << 20
+
+
+def flops(M, K, N):
+    return 2.0 * M * N * K
+
+
+def h100_reference_tflops():
+    return sum(flops(*s) for s in SHAPES) / (sum(H100_TORCH_US) * 1e-6) / 1e12
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK), "fallback"
+
+
+def source_hash(*rel):
+    h = hashlib.sha256()
+    for r in rel:
+        with open(os.path.join(ROOT, r), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic(kernel, current_hash):
+    """Per-launch DRAM bytes from a committed ncu summary, if it was taken on
+    the current source of the kernel (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f).get(kernel)
+    if not d or d.get("source_hash") != current_hash:
+        return None
+    return d.get("bytes_per_launch")
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.gpu)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, v in zip(self.NAMES, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------- GPU bench
+
+def run_gpu(args, rank, world, local_rank):
+    import torch
+    import fp8_scaled_gemm_mm_gb300 as fm
+    from fp8_scaled_gemm_mm_gb300 import synth
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    fm.lib()
+
+    # ---- set-up: resident inputs, weights quantized once per output channel
+    work = []
+    for i, (M, K, N) in enumerate(SHAPES):
+        X = synth.normal((M, K), 1.0, seed=synth.SEED_A + 10 * i, device=dev)
+        W = synth.normal((N, K), 0.02, seed=synth.SEED_B + 10 * i, device=dev)
+        B = torch.empty((N, K), dtype=torch.uint8, device=dev)
+        b_s = torch.empty((N, 1), dtype=torch.float32, device=dev)
+        fm.per_token_group_quant_fp8(W, B, b_s, K)
+        del W
+        A = torch.empty((M, K), dtype=torch.uint8, device=dev)
+        a_s = torch.empty((M, 1), dtype=torch.float32, device=dev)
+        D = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        work.append(dict(M=M, K=K, N=N, X=X, A=A, a_s=a_s, B=B, b_s=b_s, D=D))
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    torch.cuda.synchronize()
+
+    step_flops = sum(flops(w["M"], w["K"], w["N"]) for w in work)
+    step_quant_bytes = sum(w["M"] * w["K"] * 3 + w["M"] * 4 for w in work)
+    n_events = 2 * len(work) + 1
+
+    def step(ev):
+        ev[0].record()
+        for i, w in enumerate(work):
+            fm.per_token_group_quant_fp8(w["X"], w["A"], w["a_s"], w["K"])
+            ev[2 * i + 1].record()
+            fm.fp8_scaled_mm(w["A"], w["B"], w["a_s"], w["b_s"], fm.A_ROW | fm.B_COL, w["D"])
+            ev[2 * i + 2].record()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_events)] for _ in range(args.steps)]
+    for _ in range(args.warmup):
+        flush.zero_()
+        step([torch.cuda.Event(enable_timing=True) for _ in range(n_events)])
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local_rank if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
+    if rank == 0:
+        sampler.start()
+        time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        flush.zero_()                       # L2 flush between timed steps (not inside them)
+        step(evs[k])
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    wall = time.perf_counter() - t0
+    clocks = sampler.stop() if rank == 0 else None
+
+    step_ms, gemm_ms, quant_ms = [], [], []
+    per_shape_gemm = [0.0] * len(work)
+    for ev in evs:
+        step_ms.append(ev[0].elapsed_time(ev[-1]))
+        g = q = 0.0
+        for i in range(len(work)):
+            q += ev[2 * i].elapsed_time(ev[2 * i + 1])
+            gi = ev[2 * i + 1].elapsed_time(ev[2 * i + 2])
+            g += gi
+            per_shape_gemm[i] += gi
+        gemm_ms.append(g)
+        quant_ms.append(q)
+    tot_step_ms = sum(step_ms)
+    tot_gemm_ms = sum(gemm_ms)
+    tot_quant_ms = sum(quant_ms)
+    if world > 1:
+        t = torch.tensor([tot_step_ms, tot_gemm_ms, tot_quant_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        tot_step_ms, tot_gemm_ms, tot_quant_ms = t.tolist()
+
+    # ---- group-128 quant on its largest workload (plain and fused), rank 0 only
+    quant_obj = None
+    if rank == 0:
+        quant_obj = bench_group_quant(torch, fm, synth, dev, flush)
+
+    # ---- end to end through the C ABI with host buffers
+    e2e = None
+    if rank == 0 and not args.no_e2e:
+        e2e = bench_e2e(torch, fm, work, flush, args)
+
+    res = dict(step_ms=tot_step_ms / args.steps, gemm_ms=tot_gemm_ms / args.steps,
+               quant_ms=tot_quant_ms / args.steps, wall=wall, step_flops=step_flops,
+               step_quant_bytes=step_quant_bytes, clocks=clocks, quant=quant_obj, e2e=e2e,
+               per_shape_gemm_ms=[x / args.steps for x in per_shape_gemm], launches=2 * len(work) * args.steps)
+    return res
+
+
+def bench_group_quant(torch, fm, synth, dev, flush, reps=20):
+    M, K = QUANT_M, QUANT_K
+    out = {}
+    for name, fuse in (("plain", False), ("fused_silu_mul", True)):
+        x = synth.quant_input(M, 2 * K if fuse else K, torch.bfloat16, seed=5, device=dev)
+        q, s = fm.alloc_group_quant_outputs(M, K, 128, fm.SCALE_UE8M0_PACKED, True, device=dev)
+        for _ in range(3):
+            fm.per_token_group_quant_fp8(x, q, s, 128, fm.SCALE_UE8M0_PACKED, True, fuse)
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fm.per_token_group_quant_fp8(x, q, s, 128, fm.SCALE_UE8M0_PACKED, True, fuse)
+            b.record()
+            ts.append((a, b))
+        torch.cuda.synchronize()
+        us = statistics.median(a.elapsed_time(b) for a, b in ts) * 1e3
+        nbytes = M * K * 2 * (2 if fuse else 1) + M * K + (K // 512) * ((M + 3) // 4 * 4) * 4
+        out[name] = {"us": round(us, 2), "bytes": nbytes, "gbs": round(nbytes / (us * 1e-6) / 1e9, 1)}
+    return out
+
+
+def bench_e2e(torch, fm, work, flush, args):
+    """Same step through the C ABI from pinned host buffers: H2D of each
+    activation, quant + GEMM, D2H of each output, all inside the timed region."""
+    host_x = [torch.empty(w["X"].shape, dtype=torch.bfloat16, pin_memory=True) for w in work]
+    for hx, w in zip(host_x, work):
+        hx.copy_(w["X"].cpu())
+    host_d = [torch.empty(w["D"].shape, dtype=torch.bfloat16, pin_memory=True) for w in work]
+    h2d = sum(h.numel() * 2 for h in host_x)
+    d2h = sum(h.numel() * 2 for h in host_d)
+    steps = max(3, min(args.steps, 10))
+
+    def one():
+        for hx, hd, w in zip(host_x, host_d, work):
+            w["X"].copy_(hx, non_blocking=True)
+            fm.per_token_group_quant_fp8(w["X"], w["A"], w["a_s"], w["K"])
+            fm.fp8_scaled_mm(w["A"], w["B"], w["a_s"], w["b_s"], fm.A_ROW | fm.B_COL, w["D"])
+            hd.copy_(w["D"], non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(steps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        one()
+        torch.cuda.synchronize()
+        times.append(time.perf_counter() - t0)
+    t = statistics.median(times)
+    step_flops = sum(flops(w["M"], w["K"], w["N"]) for w in work)
+    return {"value": round(step_flops / t / 1e12, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(t * 1e3, 3), "steps": steps}
+
+
+# --------------------------------------------------------- CPU reference
+
+_ORACLE_WEIGHTS = {}
+
+
+def oracle_sample(rows_per_shape, seed=0):
+    """Run the oracle's quant + GEMM on `rows_per_shape` rows of every shape.
+    Returns (flops done, seconds, threads)."""
+    import oracle
+    from fp8_scaled_gemm_mm_gb300 import synth
+    done = 0.0
+    elapsed = 0.0
+    threads = oracle.num_threads()
+    for i, (M, K, N) in enumerate(SHAPES):
+        X = synth.to_bits(synth.normal((rows_per_shape, K), 1.0, seed=1000 + 10 * seed + i))
+        if i not in _ORACLE_WEIGHTS:              # weight preparation: once, not timed
+            W = synth.to_bits(synth.normal((N, K), 0.02, seed=2000 + i))
+            _ORACLE_WEIGHTS[i] = oracle.quantize_rows(W)
+        B, b_s = _ORACLE_WEIGHTS[i]
+        t0 = time.perf_counter()
+        A, a_s = oracle.quantize_rows(X)
+        oracle.gemm(A, B, a_s, b_s, oracle.A_ROW, oracle.B_COL, threads=threads)
+        elapsed += time.perf_counter() - t0
+        done += flops(rows_per_shape, K, N)
+    return done, elapsed, threads
+
+
+def cpu_baseline(rows_per_shape):
+    done, sec, threads = oracle_sample(rows_per_shape)
+    return {"value": round(done / sec / 1e12, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{rows_per_shape} rows of each of the 5 shapes: per-row quant + fp64 GEMM over all N "
+                      f"({done / 1e9:.1f} GFLOP, {sec:.1f} s)"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    rows = args.ref_rows
+    for _ in range(args.warmup):
+        oracle_sample(rows)
+    tot_f = tot_s = 0.0
+    threads = 1
+    t_wall = time.perf_counter()
+    for k in range(args.steps):
+        f, s, threads = oracle_sample(rows, seed=k)
+        tot_f += f
+        tot_s += s
+    wall = time.perf_counter() - t_wall
+    value = tot_f / tot_s / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tot_s / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "large rowwise FP8 prefill GEMMs + per-token activation quant (sample)",
+                   "shapes_MxKxN": [list(s) for s in SHAPES], "rows_per_shape_per_step": rows},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{rows} rows of each shape per step, all N"},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "wall_s": round(wall, 2),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--cpu-rows", type=int, default=480, help="oracle rows per shape for cpu_baseline")
+    ap.add_argument("--ref-rows", type=int, default=16, help="oracle rows per shape per reference step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import torch
+    if world > 1:
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+
+    res = run_gpu(args, rank, world, local_rank)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank != 0:
+        return 0
+
+    peaks, peak_kind = load_peaks()
+    fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
+    hbm_peak = peaks["hbm_gbs"]
+    value = world * res["step_flops"] / (res["step_ms"] * 1e-3) / 1e12
+    gemm_tflops = res["step_flops"] / (res["gemm_ms"] * 1e-3) / 1e12
+    quant_gbs = res["step_quant_bytes"] / (res["quant_ms"] * 1e-3) / 1e9
+    ghash = source_hash("fp8_scaled_gemm_mm_gb300/csrc/gemm.cu", "fp8_scaled_gemm_mm_gb300/csrc/ptx.cuh")
+    qhash = source_hash("fp8_scaled_gemm_mm_gb300/csrc/quant.cu")
+    traffic = load_traffic("gemm", ghash)
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(res["step_ms"], 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": round(value / world / h100_reference_tflops(), 3),
+        "vs_baseline_note": "per-GPU value / torch._scaled_mm on H100 80GB for the same five shapes "
+                            f"({h100_reference_tflops():.0f} TFLOP/s, pages' kernel table; other hardware)",
+        "dtype": "e4m3 x e4m3 -> fp32 accumulate -> bf16",
+        "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights, bf16, quantized on device)",
+        "config": {"workload": "large rowwise-scaled FP8 prefill GEMMs (5 shapes) + per-token activation quant",
+                   "shapes_MxKxN": [list(s) for s in SHAPES], "out": "bf16", "scales": "fp32 per-row x per-col",
+                   "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write), outside the step events",
+                   "parallelism": f"replicas x{world} (no data-path collective)"},
+        "gemm": {"tflops": round(gemm_tflops, 2), "ms_per_step": round(res["gemm_ms"], 4),
+                 "per_shape_tflops": [round(flops(*s) / (t * 1e-3) / 1e12, 1)
+                                      for s, t in zip(SHAPES, res["per_shape_gemm_ms"])]},
+        "roofline": {"bound": "tensor", "achieved": round(gemm_tflops, 2), "peak": round(fp8_peak, 1),
+                     "unit": "TFLOP/s", "frac": round(gemm_tflops / fp8_peak, 4),
+                     "traffic": traffic,
+                     "peak_note": f"{peak_kind} bf16 burst {peaks['bf16_tflops']} TFLOP/s x {FP8_OVER_BF16} "
+                                  "(nominal fp8:bf16 dense ratio)",
+                     "kernel": "fp8_gemm_kernel", "source_hash": ghash},
+        "activation_quant": {"gbs": round(quant_gbs, 1), "frac_hbm": round(quant_gbs / hbm_peak, 4),
+                             "ms_per_step": round(res["quant_ms"], 4)},
+        "group_quant": None,
+        "gpu_launches": res["launches"],
+        "clocks": res["clocks"],
+        "e2e": res["e2e"],
+        "cpu_baseline": None,
+        "wall_s": round(res["wall"], 3),
+    }
+    if res["quant"]:
+        gq = res["quant"]
+        line["group_quant"] = {
+            "workload": f"M={QUANT_M} K={QUANT_K} bf16, group 128, UE8M0 packed column-major scales",
+            "bound": "hbm", "peak_gbs": hbm_peak, "source_hash": qhash,
+            **{k: dict(v, frac=round(v["gbs"] / hbm_peak, 4)) for k, v in gq.items()}}
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_rows)
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
