@@ -289,6 +289,60 @@ def bench_e2e(torch, fm, work, flush, args):
             "d2h_bytes_per_step": d2h, "ms_per_step": round(t * 1e3, 3), "steps": steps}
 
 
+# ---------------------------------------------------- single-kernel cases
+
+def run_kernel_case(args):
+    """Launch one kernel on its workload warmup + steps times (for profilers)
+    and print its event-timed median.  gemm: a prefill shape (--shape, default
+    8320x5376x21504) or --mnk M,K,N, rowwise scales; quant / quant_fused:
+    group-128 quant of M=8192, K=7168 bf16 with UE8M0 packed column-major
+    scales."""
+    import torch
+    import fp8_scaled_gemm_mm_gb300 as fm
+    from fp8_scaled_gemm_mm_gb300 import synth
+    dev = torch.device("cuda", 0)
+    if args.kernel_case == "gemm":
+        M, K, N = SHAPES[args.shape] if not args.mnk else tuple(int(v) for v in args.mnk.split(","))
+        X = synth.normal((M, K), 1.0, seed=1, device=dev)
+        W = synth.normal((N, K), 0.02, seed=2, device=dev)
+        A = torch.empty((M, K), dtype=torch.uint8, device=dev)
+        B = torch.empty((N, K), dtype=torch.uint8, device=dev)
+        a_s = torch.empty((M, 1), dtype=torch.float32, device=dev)
+        b_s = torch.empty((N, 1), dtype=torch.float32, device=dev)
+        fm.per_token_group_quant_fp8(X, A, a_s, K)
+        fm.per_token_group_quant_fp8(W, B, b_s, K)
+        del X, W
+        D = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        work = flops(M, K, N)
+
+        def launch():
+            fm.fp8_scaled_mm(A, B, a_s, b_s, fm.A_ROW | fm.B_COL, D)
+    else:
+        fuse = args.kernel_case == "quant_fused"
+        M, K = QUANT_M, QUANT_K
+        x = synth.quant_input(M, 2 * K if fuse else K, torch.bfloat16, seed=5, device=dev)
+        q, s = fm.alloc_group_quant_outputs(M, K, 128, fm.SCALE_UE8M0_PACKED, True, device=dev)
+        work = M * K * 2 * (2 if fuse else 1) + M * K + (K // 512) * ((M + 3) // 4 * 4) * 4
+
+        def launch():
+            fm.per_token_group_quant_fp8(x, q, s, 128, fm.SCALE_UE8M0_PACKED, True, fuse)
+    for _ in range(args.warmup):
+        launch()
+    ts = []
+    for _ in range(args.steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        launch()
+        b.record()
+        ts.append((a, b))
+    torch.cuda.synchronize()
+    us = statistics.median(a.elapsed_time(b) for a, b in ts) * 1e3
+    rate = work / (us * 1e-6) / (1e12 if args.kernel_case == "gemm" else 1e9)
+    print(json.dumps({"kernel_case": args.kernel_case, "us": round(us, 2),
+                      ("tflops" if args.kernel_case == "gemm" else "gbs"): round(rate, 1)}), flush=True)
+    return 0
+
+
 # --------------------------------------------------------- CPU reference
 
 _ORACLE_WEIGHTS = {}
@@ -365,6 +419,10 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=16, help="oracle rows per shape per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--kernel-case", choices=["gemm", "quant", "quant_fused"], default=None,
+                    help="run a single kernel on its workload (for profilers) instead of the benchmark")
+    ap.add_argument("--shape", type=int, default=0, help="prefill shape index for --kernel-case gemm")
+    ap.add_argument("--mnk", default=None, help="M,K,N for --kernel-case gemm instead of a prefill shape")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -375,6 +433,8 @@ def main():
 
     if args.impl == "reference":
         return run_reference(args, rank, world)
+    if args.kernel_case:
+        return run_kernel_case(args)
 
     import torch
     if world > 1:

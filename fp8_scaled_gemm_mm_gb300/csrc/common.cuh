@@ -5,7 +5,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
-#include "../../include/fp8mm.h"
+#include "fp8mm.h"
 
 namespace fp8mm {
 

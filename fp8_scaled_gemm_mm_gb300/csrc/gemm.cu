@@ -385,6 +385,208 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ------------------------------------------------ small-M: swap-AB + split-K
+//
+// For few rows (M <= 128) the weight is what has to stream from HBM, and a
+// 128 x BN tile grid has far fewer tiles than SMs.  Here the MMA's 128-row
+// operand is a 128-row slice of the weight B and the N = BT operand is the
+// token block of A, so D^T[n, m] accumulates in TMEM (lane = n, column = m).
+// The K range of a tile is split across the S CTAs of a thread-block cluster;
+// each CTA writes its fp32 partial [BT][128] into its own shared memory
+// (reusing the drained stage ring), and after a cluster barrier CTA r sums
+// rows [r*128/S, (r+1)*128/S) of all S partials in rank order 0..S-1 through
+// distributed shared memory, scales, rounds and stores them.  One launch, no
+// global workspace, and a fixed summation order.
+
+template <int BT>
+struct SwapLayout {
+  static constexpr int W_BYTES = 128 * BK;          // weight slice per stage
+  static constexpr int X_BYTES = BT * BK;           // token block per stage
+  static constexpr int STAGES = BT <= 32 ? 5 : (BT == 64 ? 4 : 3);
+  static constexpr int RING = STAGES * (W_BYTES + X_BYTES);
+  static constexpr int PART = BT * 128 * 4;         // fp32 partial, aliases the ring
+  static constexpr int DATA = RING > PART ? RING : PART;
+  static constexpr int OFF_BAR = DATA;
+  static constexpr int NBARS = 2 * STAGES + 2;
+  static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
+  static constexpr int ALLOC = OFF_MISC + 16 + 1024;
+  static constexpr uint32_t TMEM_COLS = pow2_at_least(BT);
+  static_assert(X_BYTES % 1024 == 0, "token block must keep 1024-byte alignment");
+};
+
+struct SplitArgs {
+  int splits;     // cluster size S
+  int n_tiles;    // ceil(N / 128)
+};
+
+template <int BT>
+__global__ void __launch_bounds__(kThreads, 1)
+    fp8_gemm_swap_splitk_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                                const GemmArgs p, const SplitArgs sp, __nv_bfloat16* out) {
+  using L = SwapLayout<BT>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
+  uint64_t* empty = full + L::STAGES;
+  uint64_t* tfull = empty + L::STAGES;
+  uint64_t* drain = tfull + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int S = sp.splits;
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int n_tile = blockIdx.x / S;
+  const int m0 = blockIdx.y * BT;
+  const int n0 = n_tile * 128;
+  const int kb0 = static_cast<int>(static_cast<int64_t>(rank) * p.num_kb / S);
+  const int kb1 = static_cast<int>(static_cast<int64_t>(rank + 1) * p.num_kb / S);
+
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmX);
+    for (int s = 0; s < L::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(tfull, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, L::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  float* part = reinterpret_cast<float*>(smem);   // [BT][128], valid after the mainloop
+
+  if (warp == 0) {
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      int issued = 0;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status, p.timeout_ns)) break;
+        mbar_arrive_expect_tx(&full[stage], L::W_BYTES + L::X_BYTES);
+        uint8_t* st = smem + stage * (L::W_BYTES + L::X_BYTES);
+        tma_load_2d(&tmW, &full[stage], st, kb * BK, n0);
+        tma_load_2d(&tmX, &full[stage], st + L::W_BYTES, kb * BK, m0);
+        ++issued;
+        if (++stage == L::STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      const int outstanding = issued < L::STAGES ? issued : L::STAGES;
+      for (int j = 1; j <= outstanding; ++j) {
+        int s = static_cast<int>(stage) - j;
+        uint32_t ph = phase;
+        if (s < 0) {
+          s += L::STAGES;
+          ph ^= 1u;
+        }
+        volatile int never = 0;
+        mbar_wait(&full[s], ph, &never, p.status, p.timeout_ns);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_e4m3_f32(128, BT);
+      uint32_t stage = 0, phase = 0;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!mbar_wait(&full[stage], phase, abort_flag, p.status, p.timeout_ns)) break;
+        tc_fence_after();
+        uint8_t* st = smem + stage * (L::W_BYTES + L::X_BYTES);
+        const uint64_t adesc = smem_desc_sw128(smem_u32(st));
+        const uint64_t bdesc = smem_desc_sw128(smem_u32(st + L::W_BYTES));
+#pragma unroll
+        for (int k = 0; k < BK / UMMA_K; ++k)
+          mma_f8f6f4(tmem_base, adesc + static_cast<uint64_t>(k * UMMA_K / 16),
+                     bdesc + static_cast<uint64_t>(k * UMMA_K / 16), idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+        mma_commit(&empty[stage]);
+        if (++stage == L::STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      mma_commit(tfull);
+      mma_commit(drain);
+      volatile int never = 0;
+      mbar_wait(drain, 0, &never, p.status, p.timeout_ns);
+    }
+  } else {
+    // TMEM -> own shared-memory partial [BT][128] (lane = weight row within the tile)
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    if (mbar_wait(tfull, 0, abort_flag, p.status, p.timeout_ns)) {
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < BT / 16; ++c) {
+        uint32_t r[16];
+        tmem_ld_32x32b_x16(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + c * 16, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) part[(c * 16 + j) * 128 + row] = __uint_as_float(r[j]);
+      }
+    }
+    tc_fence_before();
+  }
+
+  __syncwarp();
+  cluster_sync_all();   // every partial of the cluster is in shared memory
+
+  if (warp >= 2) {
+    // rank r sums rows [r * rows_per, ...) of the tile, four consecutive rows per thread
+    const int t = threadIdx.x - 64;
+    const int rows_per = ((128 + S - 1) / S + 3) & ~3;
+    const int r_begin = rank * rows_per;
+    const int r_count = max(0, min(rows_per, 128 - r_begin));
+    const int quads = r_count >> 2;
+    const int mt = min(BT, p.M - m0);
+    const int total = quads * mt;
+    const uint32_t part_addr = smem_u32(part);
+    const bool no_abort = *abort_flag == 0;
+    for (int idx = t; idx < total && no_abort; idx += 128) {
+      const int m = idx / quads;
+      const int row = r_begin + 4 * (idx - m * quads);
+      const int n = n0 + row;
+      if (n >= p.N) continue;
+      const uint32_t off = static_cast<uint32_t>((m * 128 + row) * 4);
+      float4 acc = ld_dsmem_f32x4(mapa_shared(part_addr + off, 0));
+      for (int s2 = 1; s2 < S; ++s2) {
+        const float4 v = ld_dsmem_f32x4(mapa_shared(part_addr + off, static_cast<uint32_t>(s2)));
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
+      }
+      const float sa = a_scale_at(p, m0 + m, 0);
+      float sb[4], bs[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        sb[j] = p.b_mode == 0 ? __ldg(p.b_scale) : __ldg(p.b_scale + n + j);
+        bs[j] = p.bias ? __bfloat162float(p.bias[n + j]) : 0.0f;
+      }
+      const float v0 = acc.x * sa * sb[0] + bs[0], v1 = acc.y * sa * sb[1] + bs[1];
+      const float v2 = acc.z * sa * sb[2] + bs[2], v3 = acc.w * sa * sb[3] + bs[3];
+      const int64_t o = static_cast<int64_t>(m0 + m) * p.N + n;
+      *reinterpret_cast<uint2*>(out + o) = make_uint2(pack2(v0, v1, p.out_fp16), pack2(v2, v3, p.out_fp16));
+    }
+  }
+
+  __syncwarp();
+  cluster_sync_all();   // no CTA leaves while others may still read its partial
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, L::TMEM_COLS);
+  }
+}
+
 // ---------------------------------------------------------------- host side
 
 struct Config {
@@ -411,10 +613,55 @@ cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorM
 
 int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
 
-// Shape-keyed tile table.  Deterministic mode always takes the same row.
+template <int BT>
+cudaError_t launch_swap(const CUtensorMap& tw, const CUtensorMap& tx, const GemmArgs& p, int splits, void* out,
+                        cudaStream_t st) {
+  using L = SwapLayout<BT>;
+  auto kern = fp8_gemm_swap_splitk_kernel<BT>;
+  static int configured_dev = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_dev != dev) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
+    if (e != cudaSuccess) return e;
+    configured_dev = dev;
+  }
+  SplitArgs sp;
+  sp.splits = splits;
+  sp.n_tiles = ceil_div(p.N, 128);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(sp.n_tiles * splits), static_cast<unsigned>(ceil_div(p.M, BT)), 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = L::ALLOC;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(splits);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tw, tx, p, sp, static_cast<__nv_bfloat16*>(out));
+}
+
+// Split count for the small-M path: as many K slices (cluster size <= 8, at least two
+// K blocks each) as keep every CTA resident at two CTAs per SM.
+int pick_splits(int64_t M, int64_t N, int num_kb, int sms) {
+  const int64_t tiles = static_cast<int64_t>(ceil_div(N, 128)) * ceil_div(M, 128);
+  int s = 1;
+  while (s < 8 && tiles * (s + 1) <= 2LL * sms && (s + 1) * 2 <= num_kb) ++s;
+  return s;
+}
+
+// Shape-keyed tile table.  Deterministic mode picks its tile from N alone, so every M
+// (and every prefix / suffix of the rows) runs the same tile, K order and instruction.
 Config pick_config(int64_t M, int64_t N, bool deterministic, bool group_a, int sms) {
   if (group_a) return {64, 8, true};
-  if (deterministic) return {64, 8, false};
+  if (deterministic) {
+    if (N >= 1024) return {256, 4, false};
+    if (N >= 256) return {128, 6, false};
+    return {64, 8, false};
+  }
   const int mblk = ceil_div(M, BM);
   if (static_cast<int64_t>(mblk) * ceil_div(N, 256) >= sms) return {256, 4, false};
   if (static_cast<int64_t>(mblk) * ceil_div(N, 128) >= sms) return {128, 6, false};
@@ -459,6 +706,46 @@ extern "C" int fp8_scaled_mm(const void* A, const void* B, const float* a_scale,
   const int sms = num_sms();
   if (!status || sms <= 0) return FP8MM_ECUDA;
 
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  GemmArgs p;
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.num_kb = ceil_div(K, BK);
+  p.a_mode = a_mode;
+  p.b_mode = b_mode;
+  p.a_ld = a_mode == FP8MM_SCALE_A_GROUP128 ? K / 128 : (M + 3) / 4 * 4;
+  p.a_scale = a_scale;
+  p.b_scale = b_scale;
+  p.bias = static_cast<const __nv_bfloat16*>(bias);
+  p.out_fp16 = out_dtype == FP8MM_DTYPE_FP16;
+  p.status = status;
+  p.timeout_ns = kWaitTimeoutNs;
+
+  if (!deterministic && !group_a && M <= 128) {
+    // small M: swap-AB with split-K over a cluster
+    const int bt = M <= 16 ? 16 : (M <= 32 ? 32 : (M <= 64 ? 64 : 128));
+    const int splits = pick_splits(M, N, p.num_kb, sms);
+    CUtensorMap tw, tx;
+    if (!make_tma_2d(&tw, const_cast<void*>(B), CU_TENSOR_MAP_DATA_TYPE_UINT8, K, N, ldb, BK, 128,
+                     CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tma_2d(&tx, const_cast<void*>(A), CU_TENSOR_MAP_DATA_TYPE_UINT8, K, M, lda, BK, bt,
+                     CU_TENSOR_MAP_SWIZZLE_128B))
+      return FP8MM_ECUDA;
+    p.m_blocks = ceil_div(M, bt);
+    p.n_blocks = ceil_div(N, 128);
+    p.tiles = p.m_blocks * p.n_blocks;
+    p.raster = 1;
+    cudaError_t e;
+    switch (bt) {
+      case 16: e = launch_swap<16>(tw, tx, p, splits, out, st); break;
+      case 32: e = launch_swap<32>(tw, tx, p, splits, out, st); break;
+      case 64: e = launch_swap<64>(tw, tx, p, splits, out, st); break;
+      default: e = launch_swap<128>(tw, tx, p, splits, out, st); break;
+    }
+    return e == cudaSuccess ? FP8MM_OK : FP8MM_ECUDA;
+  }
+
   const Config cfg = pick_config(M, N, deterministic != 0, group_a, sms);
   CUtensorMap ta, tb, td;
   if (!make_tma_2d(&ta, const_cast<void*>(A), CU_TENSOR_MAP_DATA_TYPE_UINT8, K, M, lda, BK, BM,
@@ -470,26 +757,11 @@ extern "C" int fp8_scaled_mm(const void* A, const void* B, const float* a_scale,
                    N, M, N * 2, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
     return FP8MM_ECUDA;
 
-  GemmArgs p;
-  p.M = static_cast<int>(M);
-  p.N = static_cast<int>(N);
-  p.K = static_cast<int>(K);
-  p.num_kb = ceil_div(K, BK);
   p.m_blocks = ceil_div(M, BM);
   p.n_blocks = ceil_div(N, cfg.bn);
   p.tiles = p.m_blocks * p.n_blocks;
   p.raster = 16;
-  p.a_mode = a_mode;
-  p.b_mode = b_mode;
-  p.a_ld = a_mode == FP8MM_SCALE_A_GROUP128 ? K / 128 : (M + 3) / 4 * 4;
-  p.a_scale = a_scale;
-  p.b_scale = b_scale;
-  p.bias = static_cast<const __nv_bfloat16*>(bias);
-  p.out_fp16 = out_dtype == FP8MM_DTYPE_FP16;
-  p.status = status;
-  p.timeout_ns = kWaitTimeoutNs;
   const int grid = p.tiles < sms ? p.tiles : sms;
-  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (cfg.group_a)
     e = launch<64, 8, true>(ta, tb, td, p, grid, st);

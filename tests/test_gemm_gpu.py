@@ -124,3 +124,16 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     assert fm.get_device_status(clear=True) == fm.ETIMEOUT
     assert fm.get_device_status() == 0
     run_case(64, 256, 512, "row", "col")           # the context is still usable
+
+
+@pytest.mark.parametrize("M", [1, 2, 15, 16, 17, 31, 32, 33, 63, 64, 65, 100, 127, 128, 129])
+def test_small_m_boundaries(M):
+    # the small-M path (weights as the 128-row MMA operand, K split across a cluster)
+    # at every token-block boundary, with a ragged last weight tile
+    run_case(M, 1416, 2048, "row", "col", seed=M)
+
+
+@pytest.mark.parametrize("K", [16, 48, 128, 400, 28672])
+def test_small_m_k_extremes(K):
+    # K from a single partial K block to the largest K of the workloads
+    run_case(8, 256, K, "row", "col", seed=K, bias=True)

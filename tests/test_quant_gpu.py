@@ -160,3 +160,39 @@ def test_empty_batch_launches_nothing():
     q = torch.empty((0, 2048), dtype=torch.uint8, device=dev)
     s = torch.empty((0, 16), dtype=torch.float32, device=dev)
     fm.per_token_group_quant_fp8(x, q, s, 128)
+
+
+@pytest.mark.parametrize("dtype", [0, 1])
+def test_fused_every_16bit_gate(dtype):
+    # every finite bf16 / fp16 gate value, with up = 1 and up = -0.75, through the
+    # fused SiLU path: the kernel's exp / divide must agree with the oracle's bit for bit
+    vals = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    v = oracle.bf16_bits_to_f64(vals) if dtype == 0 else oracle.fp16_bits_to_f64(vals)
+    gates = vals[np.isfinite(v)]
+    K = 128
+    rows = (gates.size + K - 1) // K
+    g = np.zeros(rows * K, np.uint16)
+    g[:gates.size] = gates
+    g = g.reshape(rows, K)
+    for up_val in (1.0, -0.75):
+        up = np.full_like(g, synth.to_bits(torch.tensor([up_val], dtype=DT[dtype]))[0])
+        x = synth.from_bits(np.concatenate([g, up], axis=1), DT[dtype])
+        _compare(x, dtype, 128, 0, False, True)
+
+
+@pytest.mark.parametrize("dtype", [0, 1])
+@pytest.mark.parametrize("fuse", [False, True])
+def test_non_finite_inputs_follow_the_oracle(dtype, fuse):
+    # NaN / +-inf sprinkled into some groups: the absmax ignores NaN (maxNum) and
+    # keeps infinities; NaN products encode as +448 (the sanitizing clamp)
+    M, K = 48, 1024
+    x = synth.quant_input(M, 2 * K if fuse else K, DT[dtype], seed=61).float()
+    rng = np.random.default_rng(62)
+    for val in (float("nan"), float("inf"), float("-inf")):
+        r = rng.integers(0, M, 6)
+        c = rng.integers(0, x.shape[1], 6)
+        x[r, c] = val
+    x = x.to(DT[dtype])
+    for fmt, cm in ((0, False), (2, True), (1, False)):
+        _compare(x, dtype, 128, fmt, cm, fuse)
+    _compare(x, dtype, K, 0, False, fuse)
