@@ -18,7 +18,7 @@ import torch
 
 __all__ = [
     "Fp8mmError", "lib", "per_token_group_quant_fp8", "per_token_group_quant_fp8_scatter",
-    "fp8_scaled_mm", "get_device_status", "selftest_bounded_wait", "scale_shape", "scale_dtype",
+    "fp8_scaled_mm", "get_device_status", "selftest_bounded_wait", "selftest_scale_math", "scale_shape", "scale_dtype",
     "alloc_group_quant_outputs", "SCALE_FP32", "SCALE_FP32_POW2", "SCALE_UE8M0_PACKED",
     "A_TENSOR", "A_ROW", "A_GROUP128", "A_GROUP128_COLMAJOR", "B_TENSOR", "B_COL",
 ]
@@ -64,6 +64,8 @@ def lib():
         L.fp8mm_get_device_status.restype = I
         L.fp8mm_selftest_bounded_wait.argtypes = [I64, P]
         L.fp8mm_selftest_bounded_wait.restype = I
+        L.fp8mm_selftest_scale_math.argtypes = [ctypes.c_uint32, ctypes.c_uint32, P, P]
+        L.fp8mm_selftest_scale_math.restype = I
         L.fp8mm_status_string.argtypes = [I]
         L.fp8mm_status_string.restype = ctypes.c_char_p
         L.fp8mm_version.restype = I
@@ -177,6 +179,13 @@ def fp8_scaled_mm(A, B, a_scale, b_scale, scale_mode: int, out, bias=None, deter
 
 def get_device_status(device: int = -1, clear: bool = True) -> int:
     return lib().fp8mm_get_device_status(device, int(clear))
+
+
+def selftest_scale_math(bits_lo: int, bits_hi: int, counters, stream=None):
+    """Compare the quant kernels' scale arithmetic with IEEE division over a range
+    of fp32 bit patterns; adds mismatch counts to counters (int64 [3], device)."""
+    _check(lib().fp8mm_selftest_scale_math(int(bits_lo), int(bits_hi), _ptr(counters), _stream(stream)),
+           "fp8mm_selftest_scale_math")
 
 
 def selftest_bounded_wait(timeout_ns: int, stream=None):

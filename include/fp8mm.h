@@ -172,6 +172,17 @@ FP8MM_API int fp8mm_get_device_status(int device, int clear);
  */
 FP8MM_API int fp8mm_selftest_bounded_wait(int64_t timeout_ns, fp8mm_stream_t stream);
 
+/*
+ * Diagnostic: evaluate the quant kernels' per-group scale arithmetic for every
+ * fp32 value whose bit pattern lies in [bits_lo, bits_hi) (bits_hi <=
+ * 0x7F800000) and compare it with IEEE division: adds to device counters
+ * mismatches[0] (a/448), mismatches[1] (448/a) and mismatches[2] (the UE8M0
+ * exponent byte), for a = max(value, 1e-10).  `mismatches` is a device array of
+ * three unsigned 64-bit counters owned by the caller.
+ */
+FP8MM_API int fp8mm_selftest_scale_math(uint32_t bits_lo, uint32_t bits_hi, unsigned long long* mismatches,
+                                        fp8mm_stream_t stream);
+
 /* Human-readable name of a status code (static string). */
 FP8MM_API const char* fp8mm_status_string(int status);
 

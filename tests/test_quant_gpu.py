@@ -196,3 +196,14 @@ def test_non_finite_inputs_follow_the_oracle(dtype, fuse):
     for fmt, cm in ((0, False), (2, True), (1, False)):
         _compare(x, dtype, 128, fmt, cm, fuse)
     _compare(x, dtype, K, 0, False, fuse)
+
+
+def test_scale_math_matches_ieee_division_for_every_fp32():
+    # the kernels form a/448 and 448/a with corrected fused-multiply-add sequences;
+    # check them (and the UE8M0 exponent) against IEEE division for every positive
+    # finite fp32 amax
+    dev = require_gpu()
+    counters = torch.zeros(3, dtype=torch.int64, device=dev)
+    fm.selftest_scale_math(0, 0x7F800000, counters)
+    torch.cuda.synchronize()
+    assert counters.tolist() == [0, 0, 0]
