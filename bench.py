@@ -72,9 +72,9 @@ def source_hash(*rel):
     return h.hexdigest()[:16]
 
 
-def load_traffic(kernel, current_hash):
-    """Per-launch DRAM bytes from a committed ncu summary, if it was taken on
-    the current source of the kernel (else None)."""
+def load_traffic(kernel, current_hash, key="bytes_per_launch"):
+    """Per-launch DRAM bytes (read + write) from a committed ncu capture, if it
+    was taken on the current source of the kernel (else None)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -82,7 +82,7 @@ def load_traffic(kernel, current_hash):
         d = json.load(f).get(kernel)
     if not d or d.get("source_hash") != current_hash:
         return None
-    return d.get("bytes_per_launch")
+    return d.get(key)
 
 
 # ------------------------------------------------------------------ clocks
@@ -455,7 +455,7 @@ def main():
     gemm_tflops = res["step_flops"] / (res["gemm_ms"] * 1e-3) / 1e12
     quant_gbs = res["step_quant_bytes"] / (res["quant_ms"] * 1e-3) / 1e9
     ghash = source_hash("fp8_scaled_gemm_mm_gb300/csrc/gemm.cu", "fp8_scaled_gemm_mm_gb300/csrc/ptx.cuh")
-    qhash = source_hash("fp8_scaled_gemm_mm_gb300/csrc/quant.cu")
+    qhash = source_hash("fp8_scaled_gemm_mm_gb300/csrc/quant.cu", "fp8_scaled_gemm_mm_gb300/csrc/ptx.cuh")
     traffic = load_traffic("gemm", ghash)
     line = {
         "metric": METRIC,
@@ -484,6 +484,7 @@ def main():
                      "traffic": traffic,
                      "peak_note": f"{peak_kind} bf16 burst {peaks['bf16_tflops']} TFLOP/s x {FP8_OVER_BF16} "
                                   "(nominal fp8:bf16 dense ratio)",
+                     "traffic_note": "dram read+write bytes of one launch of the 8320x5376x21504 shape (ncu)",
                      "kernel": "fp8_gemm_kernel", "source_hash": ghash},
         "activation_quant": {"gbs": round(quant_gbs, 1), "frac_hbm": round(quant_gbs / hbm_peak, 4),
                              "ms_per_step": round(res["quant_ms"], 4)},
@@ -500,6 +501,9 @@ def main():
             "workload": f"M={QUANT_M} K={QUANT_K} bf16, group 128, UE8M0 packed column-major scales",
             "bound": "hbm", "peak_gbs": hbm_peak, "source_hash": qhash,
             **{k: dict(v, frac=round(v["gbs"] / hbm_peak, 4)) for k, v in gq.items()}}
+        line["group_quant"]["plain"]["traffic"] = load_traffic("group_quant", qhash)
+        line["group_quant"]["fused_silu_mul"]["traffic"] = load_traffic("group_quant", qhash,
+                                                                        "fused_bytes_per_launch")
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_rows)
     print(json.dumps(line), flush=True)
