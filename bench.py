@@ -133,6 +133,24 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# ------------------------------------------------------------ multi-rank
+
+def max_over_ranks(values, device="cpu"):
+    """Element-wise maximum of per-rank timings over the process group (every
+    rank receives the result); the job is as slow as its slowest rank."""
+    import torch
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_value(world, step_flops, step_ms):
+    """Whole-job throughput in TFLOP/s: every rank runs the same step on its own
+    GPU (replicas, weak scaling), so the job does world * step_flops per step in
+    the slowest rank's step time."""
+    return world * step_flops / (step_ms * 1e-3) / 1e12
+
+
 # ------------------------------------------------------------- GPU bench
 
 def run_gpu(args, rank, world, local_rank):
@@ -211,9 +229,7 @@ def run_gpu(args, rank, world, local_rank):
     tot_gemm_ms = sum(gemm_ms)
     tot_quant_ms = sum(quant_ms)
     if world > 1:
-        t = torch.tensor([tot_step_ms, tot_gemm_ms, tot_quant_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        tot_step_ms, tot_gemm_ms, tot_quant_ms = t.tolist()
+        tot_step_ms, tot_gemm_ms, tot_quant_ms = max_over_ranks([tot_step_ms, tot_gemm_ms, tot_quant_ms], dev)
 
     # ---- group-128 quant on its largest workload (plain and fused), rank 0 only
     quant_obj = None
@@ -451,7 +467,7 @@ def main():
     peaks, peak_kind = load_peaks()
     fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
     hbm_peak = peaks["hbm_gbs"]
-    value = world * res["step_flops"] / (res["step_ms"] * 1e-3) / 1e12
+    value = job_value(world, res["step_flops"], res["step_ms"])
     gemm_tflops = res["step_flops"] / (res["gemm_ms"] * 1e-3) / 1e12
     quant_gbs = res["step_quant_bytes"] / (res["quant_ms"] * 1e-3) / 1e9
     ghash = source_hash("fp8_scaled_gemm_mm_gb300/csrc/gemm.cu", "fp8_scaled_gemm_mm_gb300/csrc/ptx.cuh")
