@@ -15,8 +15,9 @@
 //   warps 2..5  epilogue: tcgen05.ld 32 columns at a time, scale (and bias), round to
 //               bf16/fp16, stage in swizzled shared memory, TMA store (edges clipped).
 // Two TMEM accumulators alternate so that the epilogue of tile i overlaps the
-// mainloop of tile i+1.  Tiles are visited in groups of `raster` M-blocks so that
-// the CTAs running at the same time share A and B panels in L2.
+// mainloop of tile i+1.  Tiles are visited in groups of `raster` M-blocks (sized
+// from K so that a group's A panel stays in L2) so that the CTAs running at the
+// same time share A and B panels in L2.
 //
 // Per-group A scales (one per 128-wide K block, the layout the group quant produces):
 // every K block goes to its own TMEM accumulator and the epilogue promotes it,
@@ -760,7 +761,15 @@ extern "C" int fp8_scaled_mm(const void* A, const void* B, const float* a_scale,
   p.m_blocks = ceil_div(M, BM);
   p.n_blocks = ceil_div(N, cfg.bn);
   p.tiles = p.m_blocks * p.n_blocks;
-  p.raster = 16;
+  // Raster group: as many M blocks as keep the group's A panel (rows x K bytes) within
+  // about 48 MB of the 126 MB L2, so the panel is re-read from L2, not HBM, while the
+  // group sweeps N, and B is fetched from HBM once per group.
+  {
+    int64_t fit = (48ll << 20) / (static_cast<int64_t>(BM) * K);
+    fit = fit < 8 ? 8 : fit;
+    const int64_t groups = (p.m_blocks + fit - 1) / fit;            // then balance the groups
+    p.raster = static_cast<int>((p.m_blocks + groups - 1) / groups);
+  }
   const int grid = p.tiles < sms ? p.tiles : sms;
   cudaError_t e;
   if (cfg.group_a)
