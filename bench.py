@@ -268,6 +268,32 @@ def bench_group_quant(torch, fm, synth, dev, flush, reps=20):
         us = statistics.median(a.elapsed_time(b) for a, b in ts) * 1e3
         nbytes = M * K * 2 * (2 if fuse else 1) + M * K + (K // 512) * ((M + 3) // 4 * 4) * 4
         out[name] = {"us": round(us, 2), "bytes": nbytes, "gbs": round(nbytes / (us * 1e-6) / 1e9, 1)}
+    # masked fused SiLU*up quant on the expert-parallel decode layout: 32 local experts
+    # of 256 (4096 tokens routed top-8), capacity 256 rows, K = 2048; bytes of the rows
+    # that hold tokens only
+    import numpy as np
+    E, T, KM = 32, 256, 2048
+    counts = synth.masked_counts(4096, E)
+    xm = synth.quant_input(E * T, 2 * KM, torch.bfloat16, seed=6, device=dev).reshape(E, T, 2 * KM)
+    mm = torch.from_numpy(counts).to(dev)
+    qm = torch.empty((E, T, KM), dtype=torch.uint8, device=dev)
+    sm = torch.empty(fm.masked_scale_shape(E, T, KM, 128, fm.SCALE_UE8M0_PACKED, True), dtype=torch.int32, device=dev)
+    for _ in range(3):
+        fm.silu_and_mul_masked_post_quant_fp8(xm, mm, qm, sm, 128)
+    ts = []
+    for _ in range(reps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fm.silu_and_mul_masked_post_quant_fp8(xm, mm, qm, sm, 128)
+        b.record()
+        ts.append((a, b))
+    torch.cuda.synchronize()
+    us = statistics.median(a.elapsed_time(b) for a, b in ts) * 1e3
+    rows = int(np.asarray(counts).sum())
+    nbytes = rows * KM * 5 + rows * (KM // 512) * 4
+    out["masked_silu_mul_ep_decode"] = {"us": round(us, 2), "bytes": nbytes, "gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
+                                        "workload": f"E={E} T={T} K={KM}, {rows} token rows"}
     return out
 
 

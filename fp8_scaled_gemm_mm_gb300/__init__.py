@@ -18,7 +18,7 @@ import torch
 
 __all__ = [
     "Fp8mmError", "lib", "per_token_group_quant_fp8", "per_token_group_quant_fp8_scatter",
-    "fp8_scaled_mm", "get_device_status", "selftest_bounded_wait", "selftest_scale_math", "scale_shape", "scale_dtype",
+    "fp8_scaled_mm", "silu_and_mul_masked_post_quant_fp8", "masked_scale_shape", "get_device_status", "selftest_bounded_wait", "selftest_scale_math", "scale_shape", "scale_dtype",
     "alloc_group_quant_outputs", "SCALE_FP32", "SCALE_FP32_POW2", "SCALE_UE8M0_PACKED",
     "A_TENSOR", "A_ROW", "A_GROUP128", "A_GROUP128_COLMAJOR", "B_TENSOR", "B_COL",
 ]
@@ -60,6 +60,8 @@ def lib():
         L.per_token_group_quant_fp8.restype = I
         L.per_token_group_quant_fp8_scatter.argtypes = [P, I, P, I, I64, P, P, I64, I64, I, I, I, P]
         L.per_token_group_quant_fp8_scatter.restype = I
+        L.silu_and_mul_masked_post_quant_fp8.argtypes = [P, I, P, I64, I64, I64, P, P, I, I, I, P]
+        L.silu_and_mul_masked_post_quant_fp8.restype = I
         L.fp8mm_get_device_status.argtypes = [I, I]
         L.fp8mm_get_device_status.restype = I
         L.fp8mm_selftest_bounded_wait.argtypes = [I64, P]
@@ -149,6 +151,25 @@ def per_token_group_quant_fp8_scatter(x, dst_row, q, s, group: int, ue8m0: int =
                                                  _ptr(s), M, K, group, int(ue8m0), int(bool(scale_colmajor)),
                                                  _stream(stream))
     _check(st, "per_token_group_quant_fp8_scatter")
+
+
+def masked_scale_shape(E: int, T: int, K: int, group: int, fmt: int, colmajor: bool):
+    """Shape of the scale tensor of silu_and_mul_masked_post_quant_fp8."""
+    if not colmajor:
+        return scale_shape(E * T, K, group, fmt, False)
+    G = K // group
+    cols = (G + 3) // 4 if fmt == SCALE_UE8M0_PACKED else G
+    return (E, cols, (T + 3) // 4 * 4)
+
+
+def silu_and_mul_masked_post_quant_fp8(x, masked_m, q, s, group: int, ue8m0: int = SCALE_UE8M0_PACKED,
+                                       scale_colmajor: bool = True, stream=None):
+    """x [E, T, 2K] -> q [E, T, K] and s for the first masked_m[e] rows of each expert."""
+    E, T, K2 = x.shape
+    st = lib().silu_and_mul_masked_post_quant_fp8(_ptr(x), _DTYPE_CODE[x.dtype], _ptr(masked_m), E, T, K2 // 2,
+                                                  _ptr(q), _ptr(s), group, int(ue8m0), int(bool(scale_colmajor)),
+                                                  _stream(stream))
+    _check(st, "silu_and_mul_masked_post_quant_fp8")
 
 
 # ------------------------------------------------------------------ GEMM

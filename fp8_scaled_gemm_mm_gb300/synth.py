@@ -78,6 +78,17 @@ def routing(M: int, topk: int = 8, num_experts: int = 256, seed: int = SEED_ROUT
     return dst, int(padded.sum())
 
 
+def masked_counts(tokens: int, local_experts: int, topk: int = 8, num_experts: int = 256,
+                  seed: int = SEED_ROUTING):
+    """Tokens held by each of the first `local_experts` experts after routing
+    `tokens` tokens to `topk` of `num_experts` experts (the per-expert counts of
+    an expert-parallel dispatch), int32 [local_experts]."""
+    g = _gen(seed)
+    scores = torch.rand((tokens, num_experts), generator=g)
+    experts = scores.topk(topk, dim=1).indices.reshape(-1).numpy()
+    return np.bincount(experts, minlength=num_experts)[:local_experts].astype(np.int32)
+
+
 def to_bits(t: torch.Tensor) -> np.ndarray:
     """bf16 / fp16 tensor -> numpy uint16 bit patterns (CPU copy)."""
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)

@@ -155,6 +155,27 @@ FP8MM_API int per_token_group_quant_fp8_scatter(const void* x, int x_dtype, cons
                                       fp8mm_stream_t stream);
 
 /*
+ * silu_and_mul_masked_post_quant_fp8
+ *   The fused SiLU(gate)*up group quant on the expert-major layout that an
+ *   expert-parallel MoE dispatch produces (sglang PR #33533, Speed Tests: the
+ *   fused, masked, column-packed UE8M0 path of EP-MoE decode):
+ *   x [E, T, 2K] (gate = x[e, t, :K], up = x[e, t, K:]), of which only the
+ *   first masked_m[e] rows of expert e hold tokens.  For those rows the result
+ *   is exactly per_token_group_quant_fp8 with fuse_silu_mul on x viewed as
+ *   [E*T, 2K]; all other rows of q and s are left untouched.
+ *   q        uint8 [E, T, K], device.
+ *   s        row-major: as per_token_group_quant_fp8 with E*T rows;
+ *            column-major: per expert, float [E, G, pad4(T)] or packed
+ *            int32 [E, ceil(G/4), pad4(T)].
+ *   masked_m int32 [E], device; values outside [0, T] are clamped and
+ *            recorded as FP8MM_EINVAL in the device status word.
+ *   group    32, 64 or 128.  Requirements as per_token_group_quant_fp8.
+ */
+FP8MM_API int silu_and_mul_masked_post_quant_fp8(const void* x, int x_dtype, const int32_t* masked_m, int64_t E,
+                                                 int64_t T, int64_t K, uint8_t* q, void* s, int group, int ue8m0,
+                                                 int scale_colmajor, fp8mm_stream_t stream);
+
+/*
  * Device status word of `device` (the current device if device < 0):
  * FP8MM_OK, or the first error a kernel recorded there (FP8MM_ETIMEOUT,
  * FP8MM_EINVAL).  Reading synchronizes with the device.  clear != 0 resets

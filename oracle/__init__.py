@@ -232,6 +232,47 @@ def group_quant_scatter(x_bits, x_dtype: int, group: int, dst_row, num_dst_rows:
     return qd, layout_scales(s, e, fmt, colmajor, rows_total=num_dst_rows, row_map=dst)
 
 
+def masked_silu_quant(x_bits, x_dtype: int, masked_m, group: int, fmt: int = SCALE_UE8M0_PACKED,
+                      colmajor: bool = True):
+    """Masked fused SiLU*up group quant on the expert-major layout x [E, T, 2K]
+    (the EP-MoE decode path of sglang PR #33533, Speed Tests): rows t <
+    masked_m[e] of expert e get the fused group quant of that row; others stay 0.
+
+    Returns (q uint8 [E, T, K], scales): row-major scales as group_quant with
+    E*T rows; column-major per expert, [E, G or ceil(G/4), pad4(T)].
+    """
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    E, T, K2 = x.shape
+    K = K2 // 2
+    G = K // group
+    q = np.zeros((E, T, K), np.uint8)
+    s_all = np.zeros((E, T, G), np.float32)
+    e_all = np.zeros((E, T, G), np.uint8)
+    written = np.zeros((E, T), bool)
+    for e in range(E):
+        n = int(masked_m[e])
+        if n <= 0:
+            continue
+        qe, se, ee = group_quant_canonical(x[e, :n], x_dtype, group, True, fmt != SCALE_FP32)
+        q[e, :n] = qe
+        s_all[e, :n] = se
+        e_all[e, :n] = ee
+        written[e, :n] = True
+    if not colmajor:
+        flat_s = s_all.reshape(E * T, G)
+        flat_e = e_all.reshape(E * T, G)
+        lay = layout_scales(flat_s, flat_e, fmt, False)
+        lay[~written.reshape(-1)] = 0
+        return q, lay
+    outs = []
+    for e in range(E):
+        lay = layout_scales(s_all[e], e_all[e], fmt, True)     # [cols, pad4(T)]
+        lay[:, :T][:, ~written[e]] = 0
+        lay[:, T:] = 0
+        outs.append(lay)
+    return q, np.stack(outs)
+
+
 def quantize_rows(x_bits, x_dtype: int = 0):
     """Per-row (per-output-channel) E4M3 quantization with fp32 scale
     absmax/448: the group quant with one group per row."""

@@ -210,3 +210,32 @@ def test_scatter_rows_equal_plain_rows():
             assert np.array_equal(qd[d], q[m]) and np.array_equal(sd[:, d], s[:, m])
     untouched = np.setdiff1d(np.arange(R), dst.ravel())
     assert np.all(qd[untouched] == 0) and np.all(sd[:, untouched] == 0)
+
+
+def test_masked_layout_is_the_fused_quant_of_the_valid_rows():
+    # x [E=3, T=5, 2K]: expert e holds masked_m[e] tokens; each valid row is the
+    # fused quant of that row alone, padding rows and experts with no tokens stay 0
+    E, T, K = 3, 5, 256
+    x = synth.to_bits(synth.quant_input(E * T, 2 * K, seed=71)).reshape(E, T, 2 * K)
+    masked = np.array([5, 0, 2], np.int32)
+    for fmt, cm in ((oracle.SCALE_UE8M0_PACKED, True), (oracle.SCALE_FP32, True), (oracle.SCALE_FP32, False)):
+        q, s = oracle.masked_silu_quant(x, 0, masked, 128, fmt, cm)
+        for e in range(E):
+            n = masked[e]
+            if n:
+                qr, sr = oracle.group_quant(x[e, :n], 0, 128, fmt, cm, fuse_silu_mul=True)
+                assert np.array_equal(q[e, :n], qr)
+                if cm:
+                    assert np.array_equal(s[e][:, :n], sr[:, :n])
+                else:
+                    assert np.array_equal(s[e * T:e * T + n], sr)
+            assert np.all(q[e, n:] == 0)
+        if cm:
+            assert s.shape == (E, 2 if fmt == oracle.SCALE_FP32 else 1, 8)
+            assert np.all(s[1] == 0) and np.all(s[:, :, T:] == 0)
+
+
+def test_masked_counts_sum_to_routed_tokens():
+    c = synth.masked_counts(4096, 256)
+    assert c.sum() == 4096 * 8 and c.dtype == np.int32
+    assert np.array_equal(synth.masked_counts(4096, 32), c[:32])

@@ -207,3 +207,43 @@ def test_scale_math_matches_ieee_division_for_every_fp32():
     fm.selftest_scale_math(0, 0x7F800000, counters)
     torch.cuda.synchronize()
     assert counters.tolist() == [0, 0, 0]
+
+
+def _masked_case(E, T, K, masked, dtype=0, fmt=2, cm=True, seed=81):
+    dev = require_gpu()
+    x = synth.quant_input(E * T, 2 * K, DT[dtype], seed=seed).reshape(E, T, 2 * K)
+    q = torch.full((E, T, K), SENTINEL, dtype=torch.uint8, device=dev)
+    s = torch.zeros(fm.masked_scale_shape(E, T, K, 128, fmt, cm), dtype=fm.scale_dtype(fmt), device=dev)
+    fm.silu_and_mul_masked_post_quant_fp8(x.to(dev), torch.from_numpy(masked).to(dev), q, s, 128, fmt, cm)
+    torch.cuda.synchronize()
+    status = fm.get_device_status(clear=True)
+    clamped = np.clip(masked, 0, T)
+    q_ref, s_ref = oracle.masked_silu_quant(synth.to_bits(x), dtype, clamped, 128, fmt, cm)
+    qg = bits(q)
+    valid = np.arange(T)[None, :] < clamped[:, None]
+    assert np.array_equal(qg[valid], q_ref[valid])
+    assert np.all(qg[~valid] == SENTINEL)                  # rows without tokens untouched
+    sg = bits(s)
+    if s_ref.dtype == np.float32:
+        assert np.array_equal(sg.view(np.uint32), s_ref.view(np.uint32))
+    else:
+        assert np.array_equal(sg, s_ref)
+    return status
+
+
+@pytest.mark.parametrize("dtype", [0, 1])
+@pytest.mark.parametrize("fmt,cm", [(2, True), (0, True), (0, False), (1, True)])
+def test_masked_silu_quant_ep_decode(dtype, fmt, cm):
+    # 32 local experts of 256 (tokens routed top-8), capacity 256 rows each, K = 2048
+    masked = synth.masked_counts(4096, 32)
+    assert _masked_case(32, 256, 2048, masked, dtype, fmt, cm) == 0
+
+
+def test_masked_silu_quant_edges():
+    # experts with no tokens, a full expert, a capacity that is not a multiple of 16,
+    # and a ragged K
+    masked = np.array([0, 100, 1, 37, 0, 99, 16, 17], np.int32)
+    assert _masked_case(8, 100, 640, masked, seed=82) == 0
+    # counts beyond the capacity are clamped and reported
+    masked = np.array([5, 120, 0, 100], np.int32)
+    assert _masked_case(4, 100, 512, masked, seed=83) == fm.EINVAL
