@@ -20,7 +20,8 @@ __all__ = [
     "Fp8mmError", "lib", "per_token_group_quant_fp8", "per_token_group_quant_fp8_scatter",
     "fp8_scaled_mm", "silu_and_mul_masked_post_quant_fp8", "masked_scale_shape", "get_device_status", "selftest_bounded_wait", "selftest_scale_math", "scale_shape", "scale_dtype",
     "alloc_group_quant_outputs", "SCALE_FP32", "SCALE_FP32_POW2", "SCALE_UE8M0_PACKED",
-    "A_TENSOR", "A_ROW", "A_GROUP128", "A_GROUP128_COLMAJOR", "B_TENSOR", "B_COL",
+    "A_TENSOR", "A_ROW", "A_GROUP128", "A_GROUP128_COLMAJOR", "A_GROUP128_UE8M0", "B_TENSOR", "B_COL",
+    "B_BLOCK128",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -31,8 +32,8 @@ OK, EINVAL, EALIGN, EUNSUPPORTED, ECUDA, ETIMEOUT = 0, -1, -2, -3, -4, -5
 # scale formats of the group quant
 SCALE_FP32, SCALE_FP32_POW2, SCALE_UE8M0_PACKED = 0, 1, 2
 # GEMM scale modes
-A_TENSOR, A_ROW, A_GROUP128, A_GROUP128_COLMAJOR = 0x0, 0x1, 0x2, 0x3
-B_TENSOR, B_COL = 0x00, 0x10
+A_TENSOR, A_ROW, A_GROUP128, A_GROUP128_COLMAJOR, A_GROUP128_UE8M0 = 0x0, 0x1, 0x2, 0x3, 0x4
+B_TENSOR, B_COL, B_BLOCK128 = 0x00, 0x10, 0x20
 
 _DTYPE_CODE = {torch.bfloat16: 0, torch.float16: 1}
 

@@ -49,6 +49,7 @@ struct GemmArgs {
   int raster;
   int a_mode, b_mode;
   int64_t a_ld;
+  int64_t b_ld;   // block B scales: blocks per row of blocks (K / 128)
   const float* a_scale;
   const float* b_scale;
   const __nv_bfloat16* bias;
@@ -97,13 +98,27 @@ __device__ __forceinline__ float a_scale_at(const GemmArgs& p, int row, int kb) 
     case FP8MM_SCALE_A_TENSOR: return __ldg(p.a_scale);
     case FP8MM_SCALE_A_ROW: return __ldg(p.a_scale + row);
     case FP8MM_SCALE_A_GROUP128: return __ldg(p.a_scale + static_cast<int64_t>(row) * p.a_ld + kb);
-    default: return __ldg(p.a_scale + static_cast<int64_t>(kb) * p.a_ld + row);
+    case FP8MM_SCALE_A_GROUP128_COLMAJOR: return __ldg(p.a_scale + static_cast<int64_t>(kb) * p.a_ld + row);
+    default: {
+      // UE8M0 bytes packed four per int32 word, column-major: byte kb % 4 of word (kb / 4, row)
+      const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(p.a_scale) + static_cast<int64_t>(kb >> 2) * p.a_ld + row);
+      const uint32_t e = (w >> (8 * (kb & 3))) & 0xFFu;
+      return __uint_as_float(e << 23);   // 2^(e-127); e = 0 gives 0
+    }
   }
+}
+
+// Block B scale of the 128-wide N block holding column n, K block kb.
+__device__ __forceinline__ float b_block_scale_at(const GemmArgs& p, int n, int kb) {
+  return __ldg(p.b_scale + static_cast<int64_t>(n >> 7) * p.b_ld + kb);
 }
 
 // b_scale and bias for the 32 columns n0..n0+31 (zeros beyond N).
 __device__ __forceinline__ void load_col_vectors(const GemmArgs& p, int n0, float (&sb)[32], float (&bs)[32]) {
-  if (p.b_mode == 0) {
+  if (p.b_mode == 2) {   // block scales were applied per K block
+#pragma unroll
+    for (int j = 0; j < 32; ++j) sb[j] = 1.0f;
+  } else if (p.b_mode == 0) {
     const float s = __ldg(p.b_scale);
 #pragma unroll
     for (int j = 0; j < 32; ++j) sb[j] = s;
@@ -344,7 +359,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = mbar_wait(&tfull[acc], (acc_i >> 1) & 1u, abort_flag, p.status, p.timeout_ns);
           if (!ok) break;
           tc_fence_after();
-          const float sa = a_scale_at(p, row, kb);
+          float sa = a_scale_at(p, row, kb);
+          if (p.b_mode == 2) sa *= b_block_scale_at(p, nbase, kb);
 #pragma unroll
           for (int c = 0; c < BN / 32; ++c) {
             uint32_t r[32];
@@ -680,7 +696,8 @@ extern "C" int fp8_scaled_mm(const void* A, const void* B, const float* a_scale,
   const int a_mode = scale_mode & 0xF;
   const int b_mode = (scale_mode >> 4) & 0xF;
   if (M < 0 || N < 0) return FP8MM_EINVAL;
-  if (a_mode > FP8MM_SCALE_A_GROUP128_COLMAJOR || b_mode > 1 || (scale_mode & ~0xFF)) return FP8MM_EINVAL;
+  if (a_mode > FP8MM_SCALE_A_GROUP128_UE8M0 || b_mode > 2 || (scale_mode & ~0xFF)) return FP8MM_EINVAL;
+  if (b_mode == 2 && a_mode < FP8MM_SCALE_A_GROUP128) return FP8MM_EINVAL;   // block B goes with group A
   if (out_dtype != FP8MM_DTYPE_BF16 && out_dtype != FP8MM_DTYPE_FP16) return FP8MM_EINVAL;
   if (M > 0x7fffffff || N > 0x7fffffff || K > 0x7fffffff) return FP8MM_EINVAL;
   if (K <= 0 || K % 16 != 0 || lda < K || ldb < K) return FP8MM_EINVAL;
@@ -716,6 +733,7 @@ extern "C" int fp8_scaled_mm(const void* A, const void* B, const float* a_scale,
   p.a_mode = a_mode;
   p.b_mode = b_mode;
   p.a_ld = a_mode == FP8MM_SCALE_A_GROUP128 ? K / 128 : (M + 3) / 4 * 4;
+  p.b_ld = K / 128;
   p.a_scale = a_scale;
   p.b_scale = b_scale;
   p.bias = static_cast<const __nv_bfloat16*>(bias);

@@ -76,8 +76,13 @@ enum {
   FP8MM_SCALE_A_ROW = 0x1,             /* a_scale[m], [M] */
   FP8MM_SCALE_A_GROUP128 = 0x2,        /* a_scale[m*(K/128) + g], [M, K/128] row-major */
   FP8MM_SCALE_A_GROUP128_COLMAJOR = 0x3, /* a_scale[g*pad4(M) + m], [K/128, pad4(M)] */
+  FP8MM_SCALE_A_GROUP128_UE8M0 = 0x4,  /* UE8M0 bytes packed four per int32, column-major
+                                          [ceil(K/512), pad4(M)] (the group quant's output):
+                                          a_s(m, g) = 2^(byte g%4 of word (g/4, m) - 127) */
   FP8MM_SCALE_B_TENSOR = 0x00,         /* b_scale[0] */
-  FP8MM_SCALE_B_COL = 0x10             /* b_scale[n], [N] */
+  FP8MM_SCALE_B_COL = 0x10,            /* b_scale[n], [N] */
+  FP8MM_SCALE_B_BLOCK128 = 0x20        /* b_scale[(n/128)*(K/128) + g], [ceil(N/128), K/128];
+                                          requires a per-group A mode */
 };
 
 /*
@@ -93,7 +98,9 @@ enum {
  *   out      out_dtype (FP8MM_DTYPE_BF16 / _FP16) row-major [M, N], device;
  *            must not overlap A, B, the scales or the bias.
  *   Per-group A scales (FP8MM_SCALE_A_GROUP128*): the sum is formed per
- *   128-wide K block and promoted in fp32 as sum_g a_s[m,g] * partial_g.
+ *   128-wide K block and promoted in fp32 as sum_g a_s[m,g] * partial_g; with
+ *   128 x 128 block B scales (FP8MM_SCALE_B_BLOCK128) as
+ *   sum_g a_s[m,g] * b_s[n/128,g] * partial_g (the block-scaled GEMM).
  *   deterministic != 0: batch-invariant mode -- one fixed tile shape and
  *   K-block order for every M, no split of K, zero-filled K tail; row m of
  *   the result is bit-identical for any M and any prefix / suffix split of

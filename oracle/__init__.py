@@ -44,8 +44,8 @@ SCALE_FP32_POW2 = 1
 SCALE_UE8M0_PACKED = 2
 
 # GEMM scale modes, A side (low nibble) and B side (high nibble)
-A_TENSOR, A_ROW, A_GROUP, A_GROUP_COLMAJOR = 0, 1, 2, 3
-B_TENSOR, B_COL = 0, 1
+A_TENSOR, A_ROW, A_GROUP, A_GROUP_COLMAJOR, A_GROUP_UE8M0 = 0, 1, 2, 3, 4
+B_TENSOR, B_COL, B_BLOCK = 0, 1, 2
 
 
 def lib():
@@ -281,6 +281,25 @@ def quantize_rows(x_bits, x_dtype: int = 0):
     return q, s[:, 0].copy()
 
 
+def quantize_blocks(w_bits, block: int = 128, x_dtype: int = 0):
+    """128 x 128 block quantization of a weight [N, K]: each block gets the
+    group-quant formula with the whole block as one group (scale absmax/448).
+    Returns (codes [N, K], scales float32 [ceil(N/block), K/block])."""
+    w = np.ascontiguousarray(w_bits, dtype=np.uint16)
+    N, K = w.shape
+    nb, kb = (N + block - 1) // block, K // block
+    q = np.empty((N, K), np.uint8)
+    s = np.empty((nb, kb), np.float32)
+    for i in range(nb):
+        rows = w[i * block:(i + 1) * block]
+        for j in range(kb):
+            blk = np.ascontiguousarray(rows[:, j * block:(j + 1) * block])
+            qb, sb, _ = group_quant_canonical(blk.reshape(1, -1), x_dtype, blk.size)
+            q[i * block:(i + 1) * block, j * block:(j + 1) * block] = qb.reshape(blk.shape)
+            s[i, j] = sb[0, 0]
+    return q, s
+
+
 def quantize_tensor(x_bits, x_dtype: int = 0):
     """Per-tensor E4M3 quantization with one fp32 scale absmax/448: the same
     formula with the whole tensor as one group."""
@@ -297,7 +316,9 @@ def gemm(A, B, a_scale, b_scale, a_mode: int, b_mode: int, bias_bits=None, out_d
     """Scaled FP8 GEMM: out[m, n] = round(a_s * b_s * sum_k A[m,k] B[n,k] (+ bias[n])).
 
     A: uint8 [M, lda] (first K columns used), B: uint8 [N, ldb].
-    a_scale: float32 scalar / [M] / [M, K/128] (a_mode 2) / [K/128, ld] (a_mode 3).
+    a_scale: float32 scalar / [M] / [M, K/128] (a_mode 2) / [K/128, ld] (a_mode 3) /
+    int32 packed UE8M0 words [ceil(K/512), ld] (a_mode 4).
+    b_scale: float32 scalar / [N] / [ceil(N/128), K/128] (b_mode 2, with a per-group a_mode).
     Returns out bits (uint16 [rows, N]) and, if want_exact, the fp64 value
     before rounding and sum |a_s b_s A B| (for accumulation-error bounds).
     """
@@ -306,7 +327,10 @@ def gemm(A, B, a_scale, b_scale, a_mode: int, b_mode: int, bias_bits=None, out_d
     M, lda = A.shape
     N, ldb = B.shape
     K = lda if K is None else K
-    a_s = np.ascontiguousarray(np.atleast_1d(a_scale), dtype=np.float32)
+    if a_mode == A_GROUP_UE8M0:    # packed UE8M0 words, passed through bit for bit
+        a_s = np.ascontiguousarray(np.asarray(a_scale, dtype=np.int32)).view(np.float32)
+    else:
+        a_s = np.ascontiguousarray(np.atleast_1d(a_scale), dtype=np.float32)
     b_s = np.ascontiguousarray(np.atleast_1d(b_scale), dtype=np.float32)
     a_ld = a_s.shape[1] if a_s.ndim == 2 else 0
     bias = None if bias_bits is None else np.ascontiguousarray(bias_bits, dtype=np.uint16)

@@ -44,6 +44,11 @@
  *    times 2^-18 of at most 2^17.6 magnitude, and for K <= 2^15 every partial
  *    sum stays below 2^33 * 2^18 = 2^51 < 2^53 ulps.  The result is scaled in
  *    fp64 and rounded once to bf16 / fp16 (round to nearest even).
+ *
+ *  - block scales (SURVEY's next step after the rowwise path; the pages name
+ *    the block / MXFP8 GEMM, sglang PR #42865, without detail): A carries one
+ *    scale per row and 128-wide K block, B one per 128 x 128 block, and
+ *    out = sum over K blocks g of a_s[m,g] * b_s[n/128, g] * partial_g.
  */
 #include <math.h>
 #include <pthread.h>
@@ -304,8 +309,10 @@ typedef struct {
   const uint8_t* A; int64_t lda;
   const uint8_t* B; int64_t ldb;
   int64_t M, N, K;
-  const float* a_scale; int a_mode; int64_t a_ld;  /* a_mode: 0 scalar, 1 row, 2 group row-major, 3 group col-major */
-  const float* b_scale; int b_mode;                /* b_mode: 0 scalar, 1 column */
+  const float* a_scale; int a_mode; int64_t a_ld;  /* a_mode: 0 scalar, 1 row, 2 group row-major, 3 group col-major,
+                                                      4 group UE8M0 bytes packed four per int32, col-major */
+  const float* b_scale; int b_mode;                /* b_mode: 0 scalar, 1 column, 2 per 128 x 128 block */
+  int64_t b_ld;                                    /* block scales per row of blocks (K / 128) */
   const uint16_t* bias;                            /* bf16 [N] or NULL */
   int out_dtype;                                   /* 0 bf16, 1 fp16 */
   const int64_t* rows; int64_t n_rows;             /* rows to compute (NULL: all) */
@@ -321,8 +328,18 @@ static double a_scale_at(const gemm_job* j, int64_t m, int64_t g) {
     case 0: return (double)j->a_scale[0];
     case 1: return (double)j->a_scale[m];
     case 2: return (double)j->a_scale[m * j->a_ld + g];
-    default: return (double)j->a_scale[g * j->a_ld + m];
+    case 3: return (double)j->a_scale[g * j->a_ld + m];
+    default: {
+      /* UE8M0: byte g % 4 of word (g / 4, m); scale 2^(byte - 127) */
+      const uint32_t* w = (const uint32_t*)j->a_scale;
+      uint32_t e = (w[(g / 4) * j->a_ld + m] >> (8 * (g % 4))) & 0xFFu;
+      return ldexp(1.0, (int)e - 127);
+    }
   }
+}
+
+static double b_block_scale_at(const gemm_job* j, int64_t n, int64_t g) {
+  return (double)j->b_scale[(n / 128) * j->b_ld + g];
 }
 
 static void* gemm_rows(void* arg) {
@@ -334,7 +351,7 @@ static void* gemm_rows(void* arg) {
     const uint8_t* a = j->A + m * j->lda;
     for (int64_t n = 0; n < j->N; ++n) {
       const uint8_t* b = j->B + n * j->ldb;
-      double bs = j->b_mode == 0 ? (double)j->b_scale[0] : (double)j->b_scale[n];
+      double bs = j->b_mode == 0 ? (double)j->b_scale[0] : (j->b_mode == 1 ? (double)j->b_scale[n] : 1.0);
       double val, sabs = 0.0;
       if (j->a_mode <= 1) {
         double acc = 0.0;
@@ -357,6 +374,7 @@ static void* gemm_rows(void* arg) {
             gabs += fabs(p);
           }
           double as = a_scale_at(j, m, g);
+          if (j->b_mode == 2) as *= b_block_scale_at(j, n, g);  /* exact: fp32 x fp32 fits fp64 */
           tot += as * acc;
           sabs += fabs(as) * gabs;
         }
@@ -377,13 +395,14 @@ int oracle_gemm(const uint8_t* A, int64_t lda, const uint8_t* B, int64_t ldb, in
                 int64_t K, const float* a_scale, int a_mode, int64_t a_ld, const float* b_scale,
                 int b_mode, const uint16_t* bias, int out_dtype, const int64_t* rows, int64_t n_rows,
                 uint16_t* out, double* exact, double* sumabs, int nthreads) {
+  if (b_mode == 2 && a_mode < 2) return -3;  /* block B scales go with per-group A scales */
   double lut[256];
   for (int i = 0; i < 256; ++i) lut[i] = e4m3_value((uint8_t)i);
   if (!rows) n_rows = M;
   if (nthreads <= 0) nthreads = (int)sysconf(_SC_NPROCESSORS_ONLN);
   if (nthreads < 1) nthreads = 1;
   if (nthreads > n_rows) nthreads = n_rows > 0 ? (int)n_rows : 1;
-  gemm_job base = {A, lda, B, ldb, M, N, K, a_scale, a_mode, a_ld, b_scale, b_mode, bias,
+  gemm_job base = {A, lda, B, ldb, M, N, K, a_scale, a_mode, a_ld, b_scale, b_mode, (K + 127) / 128, bias,
                    out_dtype, rows, n_rows, out, exact, sumabs, lut, 0, 0};
   gemm_job* jobs = (gemm_job*)malloc(sizeof(gemm_job) * (size_t)nthreads);
   pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * (size_t)nthreads);

@@ -84,8 +84,9 @@ def test_gemm_argument_validation(L):
     assert call(lda=256) == -1                        # lda < K
     assert call(lda=520) == -2                        # lda % 16
     assert call(N=260) == -2                          # N % 8
-    assert call(mode=0x4) == -1                       # bad A mode
-    assert call(mode=0x21) == -1                      # bad B mode
+    assert call(mode=0x5) == -1                       # bad A mode
+    assert call(mode=0x31) == -1                      # bad B mode
+    assert call(mode=0x21) == -1                      # block B scales need per-group A scales
     assert call(od=2) == -1                           # bad out dtype
     assert call(mode=0x12, K=80, lda=80, ldb=80) == -1  # group scales need K % 128
     assert call(A=f + 8) == -2                        # misaligned A

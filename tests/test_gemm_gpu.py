@@ -137,3 +137,32 @@ def test_small_m_boundaries(M):
 def test_small_m_k_extremes(K):
     # K from a single partial K block to the largest K of the workloads
     run_case(8, 256, K, "row", "col", seed=K, bias=True)
+
+
+def _block_case(M, N, K, seed, ue8m0_a=True, rows=None):
+    dev = require_gpu()
+    X = synth.to_bits(synth.normal((M, K), 1.0, seed=seed))
+    W = synth.to_bits(synth.normal((N, K), 0.02, seed=seed + 1))
+    B, b_blk = oracle.quantize_blocks(W)
+    if ue8m0_a:
+        A, a_words = oracle.group_quant(X, 0, 128, oracle.SCALE_UE8M0_PACKED, True)
+        a_dev, a_mode, o_mode, a_ref = to_dev(a_words), fm.A_GROUP128_UE8M0, oracle.A_GROUP_UE8M0, a_words
+    else:
+        A, a_f, _ = oracle.group_quant_canonical(X, 0, 128)
+        a_dev, a_mode, o_mode, a_ref = to_dev(a_f), fm.A_GROUP128, oracle.A_GROUP, a_f
+    out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    fm.fp8_scaled_mm(to_dev(A), to_dev(B), a_dev, to_dev(b_blk), a_mode | fm.B_BLOCK128, out)
+    torch.cuda.synchronize()
+    assert fm.get_device_status() == 0
+    _, exact, sumabs = oracle.gemm(A, B, a_ref, b_blk, o_mode, oracle.B_BLOCK, rows=rows, want_exact=True)
+    got = bits(out) if rows is None else bits(out[torch.from_numpy(rows).to(dev)])
+    return check_gemm(got, exact, sumabs, K, 0, f"block M{M} N{N} K{K}")
+
+
+@pytest.mark.parametrize("ue8m0_a", [True, False])
+def test_block_scaled_gemm(ue8m0_a):
+    # A 1 x 128 group scales (the group quant's UE8M0 output read directly, or fp32),
+    # B 128 x 128 block scales
+    _block_case(512, 7168, 2048, 11, ue8m0_a, rows=sample_rows(512, seed=1))
+    _block_case(300, 1000, 1024, 12, ue8m0_a)
+    _block_case(1, 136, 256, 13, ue8m0_a)

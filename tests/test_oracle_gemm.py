@@ -132,3 +132,34 @@ def test_fp16_output_rounding():
     A, B = _codes(rng, (4, 128)), _codes(rng, (8, 128))
     o, e, _ = oracle.gemm(A, B, np.float32(1e-3), np.float32(1), 0, 0, out_dtype=1, want_exact=True)
     assert np.array_equal(o, e.astype(np.float16).view(np.uint16))
+
+
+def test_block_scales_and_packed_ue8m0_a_scales():
+    # per-group A scales x 128 x 128 block B scales: with powers of two the result is
+    # exact and equals sum_g a[m,g] b[n/128,g] partial_g computed here in int64
+    rng = np.random.default_rng(6)
+    M, N, K = 5, 300, 384
+    G = K // 128
+    A, B = _codes(rng, (M, K)), _codes(rng, (N, K))
+    ea = rng.integers(120, 134, size=(M, G))                  # UE8M0 exponent bytes
+    eb = rng.integers(-3, 4, size=((N + 127) // 128, G))
+    a_f = (2.0 ** (ea - 127)).astype(np.float32)
+    b_blk = (2.0 ** eb).astype(np.float32)
+    _, e1, _ = oracle.gemm(A, B, a_f, b_blk, oracle.A_GROUP, oracle.B_BLOCK, want_exact=True)
+    IA, IB = _int_form(A), _int_form(B)
+    want = np.zeros((M, N))
+    for g in range(G):
+        part = (IA[:, g * 128:(g + 1) * 128] @ IB[:, g * 128:(g + 1) * 128].T).astype(np.float64) / 2.0 ** 18
+        want += part * (2.0 ** (ea[:, g] - 127))[:, None] * (2.0 ** eb[np.arange(N) // 128, g])[None, :]
+    assert np.array_equal(e1, want)
+    # the same A scales as packed UE8M0 words, column-major [ceil(G/4), pad4(M)]
+    words = np.zeros(((G + 3) // 4, oracle.pad4(M)), np.uint32)
+    for g in range(G):
+        words[g // 4, :M] |= ea[:, g].astype(np.uint32) << np.uint32(8 * (g % 4))
+    _, e2, _ = oracle.gemm(A, B, words.view(np.int32), b_blk, oracle.A_GROUP_UE8M0, oracle.B_BLOCK, want_exact=True)
+    assert np.array_equal(e1, e2)
+    # block scales constant over N blocks reduce to the column-scale-free group mode
+    _, e3, _ = oracle.gemm(A, B, a_f, np.ones(((N + 127) // 128, G), np.float32), oracle.A_GROUP, oracle.B_BLOCK,
+                           want_exact=True)
+    _, e4, _ = oracle.gemm(A, B, a_f, np.float32(1), oracle.A_GROUP, oracle.B_TENSOR, want_exact=True)
+    assert np.array_equal(e3, e4)

@@ -239,3 +239,19 @@ def test_masked_counts_sum_to_routed_tokens():
     c = synth.masked_counts(4096, 256)
     assert c.sum() == 4096 * 8 and c.dtype == np.int32
     assert np.array_equal(synth.masked_counts(4096, 32), c[:32])
+
+
+def test_block_quant_is_groupwise_per_block():
+    # each 128 x 128 block: absmax/448 scale, its largest element at +-448, and the
+    # same codes as the group quant of the block taken as one row
+    w = synth.to_bits(synth.normal((200, 256), 0.02, seed=91))
+    q, s = oracle.quantize_blocks(w)
+    assert q.shape == (200, 256) and s.shape == (2, 2)
+    v = oracle.bf16_bits_to_f64(w)
+    for i in range(2):
+        for j in range(2):
+            blk = v[i * 128:(i + 1) * 128, j * 128:(j + 1) * 128]
+            a = np.abs(blk).max()
+            assert abs(s[i, j] - a / 448) <= a / 448 * 2.0 ** -23
+            deq = oracle.e4m3_decode(q[i * 128:(i + 1) * 128, j * 128:(j + 1) * 128])
+            assert np.abs(deq).max() == 448.0
