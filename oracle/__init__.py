@@ -300,6 +300,35 @@ def quantize_blocks(w_bits, block: int = 128, x_dtype: int = 0):
     return q, s
 
 
+def static_quant(x_bits, x_dtype: int, scale):
+    """Static per-tensor activation quant with a given fp32 scale (the prhub
+    summary of sglang PR #33148, Key source snippets: the checkpoint's activation
+    scale input_scale.max() is used as it is): q = E4M3(fl32(x / scale))."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    v = (bf16_bits_to_f64(x) if x_dtype == 0 else fp16_bits_to_f64(x)).astype(np.float32)
+    with np.errstate(over="ignore", divide="ignore", invalid="ignore"):
+        r = v / np.float32(scale)                     # IEEE fp32 division
+    return e4m3_encode(r)
+
+
+def requantize_with_max_scale(w_codes, shard_scales, logical_widths):
+    """Fused weight with per-logical-shard scales -> one per-tensor scale (same
+    snippets: process_weights_after_loading): s_max = max_i s_i and every row of
+    shard i becomes E4M3(fl32(fl32(decode(q) * s_i) / s_max)).
+    Returns (codes, s_max)."""
+    w = np.ascontiguousarray(w_codes, dtype=np.uint8)
+    s = np.asarray(shard_scales, dtype=np.float32)
+    s_max = np.float32(s.max())
+    out = np.empty_like(w)
+    start = 0
+    for i, width in enumerate(logical_widths):
+        deq = (e4m3_decode(w[start:start + width]).astype(np.float32) * s[i]).astype(np.float32)
+        out[start:start + width] = e4m3_encode((deq / s_max).astype(np.float32))
+        start += width
+    out[start:] = w[start:]
+    return out, s_max
+
+
 def quantize_tensor(x_bits, x_dtype: int = 0):
     """Per-tensor E4M3 quantization with one fp32 scale absmax/448: the same
     formula with the whole tensor as one group."""

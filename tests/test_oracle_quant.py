@@ -255,3 +255,31 @@ def test_block_quant_is_groupwise_per_block():
             assert abs(s[i, j] - a / 448) <= a / 448 * 2.0 ** -23
             deq = oracle.e4m3_decode(q[i * 128:(i + 1) * 128, j * 128:(j + 1) * 128])
             assert np.abs(deq).max() == 448.0
+
+
+def test_static_quant_pins():
+    x = synth.to_bits(synth.normal((4, 512), 3.0, seed=92))
+    v = oracle.bf16_bits_to_f64(x)
+    # scale 1: the codes are the encoding of the values themselves
+    assert np.array_equal(oracle.static_quant(x, 0, 1.0), oracle.e4m3_encode(v.astype(np.float32)))
+    # a power-of-two scale divides exactly
+    assert np.array_equal(oracle.static_quant(x, 0, 0.25), oracle.e4m3_encode((v * 4).astype(np.float32)))
+    # beyond the range the codes saturate to +-448
+    q = oracle.static_quant(x, 0, 1e-3)
+    assert np.all(np.abs(oracle.e4m3_decode(q)) <= 448) and np.any((q & 0x7F) == 0x7E)
+
+
+def test_requantize_with_max_scale_pins():
+    rng = np.random.default_rng(93)
+    w = rng.integers(0, 256, size=(96, 64), dtype=np.uint8)
+    w[(w & 0x7F) == 0x7F] = 0x30
+    widths = [32, 48, 16]
+    # equal shard scales: nothing changes
+    out, smax = oracle.requantize_with_max_scale(w, [0.5, 0.5, 0.5], widths)
+    assert np.array_equal(out, w) and smax == np.float32(0.5)
+    # a shard whose scale is s_max / 4: its values are divided by 4 exactly, then re-encoded
+    out, smax = oracle.requantize_with_max_scale(w, [1.0, 0.25, 1.0], widths)
+    assert smax == 1.0
+    assert np.array_equal(out[:32], w[:32]) and np.array_equal(out[80:], w[80:])
+    mid = oracle.e4m3_decode(w[32:80]) / 4
+    assert np.array_equal(out[32:80], oracle.e4m3_encode(mid.astype(np.float32)))
