@@ -18,7 +18,8 @@ import torch
 
 __all__ = [
     "Fp8mmError", "lib", "per_token_group_quant_fp8", "per_token_group_quant_fp8_scatter",
-    "fp8_scaled_mm", "silu_and_mul_masked_post_quant_fp8", "masked_scale_shape", "get_device_status", "selftest_bounded_wait", "selftest_scale_math", "scale_shape", "scale_dtype",
+    "fp8_scaled_mm", "silu_and_mul_masked_post_quant_fp8", "static_per_tensor_quant_fp8",
+    "requantize_with_max_scale_fp8", "masked_scale_shape", "get_device_status", "selftest_bounded_wait", "selftest_scale_math", "scale_shape", "scale_dtype",
     "alloc_group_quant_outputs", "SCALE_FP32", "SCALE_FP32_POW2", "SCALE_UE8M0_PACKED",
     "A_TENSOR", "A_ROW", "A_GROUP128", "A_GROUP128_COLMAJOR", "A_GROUP128_UE8M0", "B_TENSOR", "B_COL",
     "B_BLOCK128",
@@ -63,6 +64,10 @@ def lib():
         L.per_token_group_quant_fp8_scatter.restype = I
         L.silu_and_mul_masked_post_quant_fp8.argtypes = [P, I, P, I64, I64, I64, P, P, I, I, I, P]
         L.silu_and_mul_masked_post_quant_fp8.restype = I
+        L.static_per_tensor_quant_fp8.argtypes = [P, I, P, P, I64, P]
+        L.static_per_tensor_quant_fp8.restype = I
+        L.requantize_with_max_scale_fp8.argtypes = [P, P, P, P, I, I64, I64, P, P]
+        L.requantize_with_max_scale_fp8.restype = I
         L.fp8mm_get_device_status.argtypes = [I, I]
         L.fp8mm_get_device_status.restype = I
         L.fp8mm_selftest_bounded_wait.argtypes = [I64, P]
@@ -171,6 +176,28 @@ def silu_and_mul_masked_post_quant_fp8(x, masked_m, q, s, group: int, ue8m0: int
                                                   _ptr(q), _ptr(s), group, int(ue8m0), int(bool(scale_colmajor)),
                                                   _stream(stream))
     _check(st, "silu_and_mul_masked_post_quant_fp8")
+
+
+def static_per_tensor_quant_fp8(x, scale, q, stream=None):
+    """q = E4M3(x / scale[0]) elementwise (static activation scale)."""
+    st = lib().static_per_tensor_quant_fp8(_ptr(x), _DTYPE_CODE[x.dtype], _ptr(scale), _ptr(q), x.numel(),
+                                           _stream(stream))
+    _check(st, "static_per_tensor_quant_fp8")
+
+
+def requantize_with_max_scale_fp8(w, shard_scales, logical_widths, w_out=None, max_scale_out=None, stream=None):
+    """Bring a fused weight's per-shard scales to their maximum; returns (w_out, s_max tensor [1])."""
+    N, K = w.shape
+    if w_out is None:
+        w_out = w
+    if max_scale_out is None:
+        max_scale_out = torch.empty(1, dtype=torch.float32, device=w.device)
+    widths = (ctypes.c_int64 * len(logical_widths))(*[int(v) for v in logical_widths])
+    st = lib().requantize_with_max_scale_fp8(_ptr(w), _ptr(w_out), _ptr(shard_scales),
+                                             ctypes.cast(widths, ctypes.c_void_p), len(logical_widths), N, K,
+                                             _ptr(max_scale_out), _stream(stream))
+    _check(st, "requantize_with_max_scale_fp8")
+    return w_out, max_scale_out
 
 
 # ------------------------------------------------------------------ GEMM

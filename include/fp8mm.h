@@ -183,6 +183,34 @@ FP8MM_API int silu_and_mul_masked_post_quant_fp8(const void* x, int x_dtype, con
                                                  int scale_colmajor, fp8mm_stream_t stream);
 
 /*
+ * static_per_tensor_quant_fp8
+ *   Static per-tensor activation quant with a given scale (the checkpoint's
+ *   activation scale, prhub summary of sglang PR #33148, Key source snippets):
+ *   q[i] = E4M3FN_rne_satfinite(fl32(x[i] / scale[0])), IEEE division; a NaN
+ *   quotient encodes as +448.
+ *   x      bf16 / fp16 [numel], device, 16-byte aligned; numel % 16 == 0.
+ *   scale  fp32 [1], device.   q  uint8 [numel], device, 16-byte aligned.
+ */
+FP8MM_API int static_per_tensor_quant_fp8(const void* x, int x_dtype, const float* scale, uint8_t* q, int64_t numel,
+                                          fp8mm_stream_t stream);
+
+/*
+ * requantize_with_max_scale_fp8
+ *   A fused weight (e.g. QKV or gate/up) whose logical shards carry their own
+ *   per-tensor scales is brought to one scale, the largest (same snippets,
+ *   process_weights_after_loading): s_max = max_i shard_scales[i]; every row of
+ *   shard i becomes E4M3(fl32(fl32(decode(w) * s_i) / s_max)); rows past the
+ *   last shard are copied.  s_max is written to max_scale_out[0].
+ *   w, w_out        uint8 E4M3 codes [N, K], device, 16-byte aligned (w_out may be w).
+ *   shard_scales    fp32 [num_shards], device.
+ *   logical_widths  int64 [num_shards], HOST; rows of each shard in order, sum <= N.
+ *   num_shards      1 .. 16.   K % 16 == 0.
+ */
+FP8MM_API int requantize_with_max_scale_fp8(const uint8_t* w, uint8_t* w_out, const float* shard_scales,
+                                            const int64_t* logical_widths, int num_shards, int64_t N, int64_t K,
+                                            float* max_scale_out, fp8mm_stream_t stream);
+
+/*
  * Device status word of `device` (the current device if device < 0):
  * FP8MM_OK, or the first error a kernel recorded there (FP8MM_ETIMEOUT,
  * FP8MM_EINVAL).  Reading synchronizes with the device.  clear != 0 resets
