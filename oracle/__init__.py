@@ -63,6 +63,8 @@ def lib():
         L.oracle_exp_f32.argtypes = [P, P, I64]
         L.oracle_silu_f32.argtypes = [P, P, I64]
         L.oracle_group_quant.argtypes = [P, I, I64, I64, I64, I, I, P, P, P]
+        L.oracle_encode_i8.argtypes = [P, P, I64]
+        L.oracle_group_quant_int8.argtypes = [P, I, I64, I64, I64, I, P, P]
         L.oracle_group_quant.restype = I
         L.oracle_gemm.argtypes = [P, I64, P, I64, I64, I64, I64, P, I, I64, P, I, P, I, P, I64,
                                   P, P, P, I]
@@ -162,6 +164,50 @@ def group_quant_canonical(x_bits, x_dtype: int, group: int, fuse_silu_mul: bool 
     if rc != 0:
         raise RuntimeError(f"oracle_group_quant failed ({rc})")
     return q, s, e
+
+
+def i8_encode(x) -> np.ndarray:
+    """fp32 -> int8: NaN -> +127, clamp to [-128, 127], round half to even."""
+    v = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(v.shape, np.int8)
+    lib().oracle_encode_i8(_ptr(v), _ptr(out), v.size)
+    return out
+
+
+def group_quant_int8(x_bits, x_dtype: int, group: int, colmajor: bool = False, fuse_silu_mul: bool = False):
+    """int8 per-token group quant (fp32 scales max(amax, 1e-10)/127).
+    Returns (q int8 [M, K], scales laid out row-major [M, G] or column-major
+    [G, pad4(M)])."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    M = x.shape[0]
+    K = x.shape[1] // 2 if fuse_silu_mul else x.shape[1]
+    if K % group:
+        raise ValueError("group must divide K")
+    q = np.empty((M, K), np.int8)
+    s = np.empty((M, K // group), np.float32)
+    rc = lib().oracle_group_quant_int8(_ptr(x), x_dtype, M, K, group, int(fuse_silu_mul), _ptr(q), _ptr(s))
+    if rc != 0:
+        raise RuntimeError(f"oracle_group_quant_int8 failed ({rc})")
+    return q, layout_scales(s, None, SCALE_FP32, colmajor)
+
+
+def group_quant_row_padded(x_bits, x_dtype: int, group: int, m_pad: int, fmt: int = SCALE_FP32,
+                           colmajor: bool = True):
+    """Row-padded group quant: outputs sized for m_pad >= M rows; rows M..m_pad-1
+    get zero codes and zero scales (the row padding plus tail zeroing of the
+    entry-point dedup notes of sglang PR #33533)."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    M, K = x.shape
+    if m_pad < M:
+        raise ValueError("m_pad < M")
+    q, s, e = group_quant_canonical(x, x_dtype, group, False, fmt != SCALE_FP32)
+    qp = np.zeros((m_pad, K), np.uint8)
+    qp[:M] = q
+    sp = np.zeros((m_pad, s.shape[1]), np.float32)
+    sp[:M] = s
+    ep = np.zeros((m_pad, s.shape[1]), np.uint8)
+    ep[:M] = e
+    return qp, layout_scales(sp, ep, fmt, colmajor)
 
 
 def pad4(n: int) -> int:

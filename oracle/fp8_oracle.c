@@ -36,6 +36,13 @@
  *    fixed sequence of IEEE fp32 operations so that a GPU that performs the
  *    same sequence reproduces it bit for bit.
  *
+ *  - int8 group quant, the third output format of the same kernel family
+ *    (same PR, "Verified": fp32 / ue8m0 / int8 scale formats): the same steps
+ *    with 127 in place of 448, fp32 scales s = fl32(a / 127), multiplier
+ *    fl32(127 / a), and q = int8(v * mult) after the same sanitizing clamp
+ *    (NaN -> +127, then [-128, 127]) and rounding to nearest, ties to even.
+ *    The pages print no int8 rounding rule; ties-to-even is the reading taken.
+ *
  *  - scaled FP8 GEMM (sglang PR #34318 "Route large SM90 row/column-scaled
  *    FP8 GEMMs to Torch", Summary; prhub summary of sglang PR #33148,
  *    "Features and motivation"): D[m,n] = out(a_s * b_s * sum_k A[m,k] B[n,k]
@@ -295,6 +302,51 @@ int oracle_group_quant(const uint16_t* x, int x_dtype, int64_t M, int64_t K, int
       for (int64_t i = 0; i < group; ++i) q[m * K + g * group + i] = e4m3_encode(v[i] * mult);
       s[m * G + g] = sc;
       e[m * G + g] = eb;
+    }
+  }
+  free(v);
+  return 0;
+}
+
+/* int8 code of an fp32 value: NaN -> +127 (the clamp's min(v, 127) comes
+   first), clamp to [-128, 127], round to nearest with ties to even. */
+static int8_t i8_encode(float x) {
+  if (isnan(x)) return 127;
+  double c = (double)x;
+  if (c > 127.0) c = 127.0;
+  if (c < -128.0) c = -128.0;
+  double f = floor(c), r = c - f;
+  double n = f;
+  if (r > 0.5 || (r == 0.5 && fmod(f, 2.0) != 0.0)) n = f + 1.0;
+  return (int8_t)n;
+}
+
+void oracle_encode_i8(const float* x, int8_t* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = i8_encode(x[i]);
+}
+
+int oracle_group_quant_int8(const uint16_t* x, int x_dtype, int64_t M, int64_t K, int64_t group,
+                            int fuse_silu_mul, int8_t* q, float* s) {
+  if (group <= 0 || K % group != 0) return -1;
+  int64_t G = K / group;
+  int64_t ldx = fuse_silu_mul ? 2 * K : K;
+  float* v = (float*)malloc(sizeof(float) * (size_t)group);
+  if (!v) return -2;
+  for (int64_t m = 0; m < M; ++m) {
+    for (int64_t g = 0; g < G; ++g) {
+      for (int64_t i = 0; i < group; ++i) {
+        int64_t k = g * group + i;
+        if (fuse_silu_mul)
+          v[i] = silu_f32(load_x(x, x_dtype, m * ldx + k)) * load_x(x, x_dtype, m * ldx + K + k);
+        else
+          v[i] = load_x(x, x_dtype, m * ldx + k);
+      }
+      float amax = 0.0f;
+      for (int64_t i = 0; i < group; ++i) amax = fmaxf(amax, fabsf(v[i]));
+      float a = fmaxf(amax, 1e-10f);
+      float mult = 127.0f / a;
+      for (int64_t i = 0; i < group; ++i) q[m * K + g * group + i] = i8_encode(v[i] * mult);
+      s[m * G + g] = a / 127.0f;
     }
   }
   free(v);

@@ -283,3 +283,67 @@ def test_requantize_with_max_scale_pins():
     assert np.array_equal(out[:32], w[:32]) and np.array_equal(out[80:], w[80:])
     mid = oracle.e4m3_decode(w[32:80]) / 4
     assert np.array_equal(out[32:80], oracle.e4m3_encode(mid.astype(np.float32)))
+
+
+def test_int8_encode_pins():
+    # ties go to the even neighbour; the clamp takes NaN to +127 and saturates
+    x = np.array([0.5, 1.5, 2.5, -0.5, -2.5, 126.5, 127.49, 300.0, -300.0, np.nan, np.inf, -np.inf, -127.5],
+                 np.float32)
+    want = np.array([0, 2, 2, 0, -2, 126, 127, 127, -128, 127, 127, -128, -128], np.int8)
+    assert np.array_equal(oracle.i8_encode(x), want)
+    # finite values in range reduce to numpy's round-half-to-even
+    r = (np.random.default_rng(94).standard_normal(20000) * 60).astype(np.float32)
+    r[::7] = np.round(r[::7]) + 0.5
+    assert np.array_equal(oracle.i8_encode(r), np.clip(np.rint(r), -128, 127).astype(np.int8))
+
+
+def test_int8_group_quant_properties():
+    x = synth.to_bits(synth.quant_input(64, 1024, seed=95))
+    v = oracle.bf16_bits_to_f64(x)
+    q, s = oracle.group_quant_int8(x, 0, 128)
+    assert q.dtype == np.int8 and s.shape == (64, 8)
+    g = v.reshape(64, 8, 128)
+    a = np.maximum(np.abs(g).max(axis=2), 1e-10)
+    # scale = absmax / 127 to fp32 rounding, and the same absmax as the fp8 quant sees
+    assert np.all(np.abs(s - a / 127) <= a / 127 * 2.0 ** -23)
+    _, s8, _ = oracle.group_quant_canonical(x, 0, 128)
+    assert np.all(np.abs(s * 127.0 - s8 * 448.0) <= a * 2.0 ** -21)
+    qg = q.reshape(64, 8, 128).astype(np.int64)
+    nz = np.abs(g).max(axis=2) > 0
+    # the largest element of every non-zero group maps to +-127, all codes within it
+    assert np.all(np.abs(qg).max(axis=2)[nz] == 127) and np.all(np.abs(qg) <= 127)
+    # dequantization is within half a step (plus the multiplier's rounding)
+    err = np.abs(qg * s[:, :, None] - g)
+    assert np.all(err <= s[:, :, None] * (0.5 + 2.0 ** -16))
+    # an all-zero group: zero codes, floor scale
+    z = np.zeros((1, 128), np.uint16)
+    qz, sz = oracle.group_quant_int8(z, 0, 128)
+    assert not qz.any() and sz[0, 0] == np.float32(np.float32(1e-10) / np.float32(127))
+    # negating the input negates the codes
+    qn, sn = oracle.group_quant_int8(x ^ np.uint16(0x8000), 0, 128)
+    assert np.array_equal(qn, -q) and np.array_equal(sn, s)
+    # column-major scales are the transpose, padded to a multiple of 4 rows
+    _, scm = oracle.group_quant_int8(x[:6], 0, 128, colmajor=True)
+    assert scm.shape == (8, 8) and np.array_equal(scm[:, :6], s[:6].T) and not scm[:, 6:].any()
+
+
+def test_int8_fused_silu_mul_against_fp64():
+    x = synth.to_bits(synth.normal((8, 512), 2.0, seed=96))
+    q, s = oracle.group_quant_int8(x, 0, 128, fuse_silu_mul=True)
+    v = oracle.bf16_bits_to_f64(x)
+    gate, up = v[:, :256], v[:, 256:]
+    ref = gate / (1.0 + np.exp(-gate)) * up
+    err = np.abs(q.astype(np.float64).reshape(8, 2, 128) * s[:, :, None] - ref.reshape(8, 2, 128))
+    assert np.all(err <= s[:, :, None] * (0.5 + 2.0 ** -12))
+
+
+def test_row_padded_pins():
+    x = synth.to_bits(synth.quant_input(10, 512, seed=97))
+    for fmt, cm in [(oracle.SCALE_FP32, True), (oracle.SCALE_FP32, False), (oracle.SCALE_UE8M0_PACKED, True)]:
+        q, sc = oracle.group_quant(x, 0, 128, fmt, cm)
+        qp, scp = oracle.group_quant_row_padded(x, 0, 128, 16, fmt, cm)
+        assert qp.shape == (16, 512) and np.array_equal(qp[:10], q) and not qp[10:].any()
+        if cm:
+            assert scp.shape[1] == 16 and np.array_equal(scp[:, :10], sc[:, :10]) and not scp[:, 10:].any()
+        else:
+            assert scp.shape[0] == 16 and np.array_equal(scp[:10], sc) and not scp[10:].any()
