@@ -22,7 +22,8 @@
  *
  *  - per-token group quant (same PR, section 1 and the commit notes on the
  *    compile-time floor): per group of g consecutive elements of a row,
- *      amax = max |v|,   a = max(amax, 1e-10),
+ *      amax = max |v| over the group's non-NaN elements (the method's
+ *             absmax ignores NaN and keeps infinities),  a = max(amax, 1e-10),
  *      s = fl32(a / 448),  mult = fl32(448 / a)      (IEEE division),
  *      UE8M0: e = biased exponent of s (+1 if its mantissa is non-zero),
  *             s = 2^(e-127), mult = 2^(127-e)       (power of two),
@@ -259,6 +260,16 @@ void oracle_silu_f32(const float* x, float* out, int64_t n) {
  * Laying the scales out (row / column major, packing) is left to the
  * caller, which does it with plain indexing.
  * x is [M, K] (fuse == 0) or [M, 2K] with gate = x[:, :K], up = x[:, K:]. */
+/* One step of the group absmax: |v| joins the maximum unless v is a NaN.  Every
+   NaN is skipped, quiet or signaling; C's fmaxf may return NaN for a signaling
+   operand (IEEE 754-2008 maxNum), which would make the result depend on where
+   the NaN sits in the group. */
+static float absmax_step(float amax, float v) {
+  if (isnan(v)) return amax;
+  float a = fabsf(v);
+  return a > amax ? a : amax;
+}
+
 int oracle_group_quant(const uint16_t* x, int x_dtype, int64_t M, int64_t K, int64_t group,
                        int fuse_silu_mul, int ue8m0, uint8_t* q, float* s, uint8_t* e) {
   if (group <= 0 || K % group != 0) return -1;
@@ -281,7 +292,7 @@ int oracle_group_quant(const uint16_t* x, int x_dtype, int64_t M, int64_t K, int
       }
       /* step 2: group absmax and the floor */
       float amax = 0.0f;
-      for (int64_t i = 0; i < group; ++i) amax = fmaxf(amax, fabsf(v[i]));
+      for (int64_t i = 0; i < group; ++i) amax = absmax_step(amax, v[i]);
       float a = fmaxf(amax, 1e-10f);
       /* step 3: scale and multiplier */
       float sc = a / 448.0f;
@@ -342,7 +353,7 @@ int oracle_group_quant_int8(const uint16_t* x, int x_dtype, int64_t M, int64_t K
           v[i] = load_x(x, x_dtype, m * ldx + k);
       }
       float amax = 0.0f;
-      for (int64_t i = 0; i < group; ++i) amax = fmaxf(amax, fabsf(v[i]));
+      for (int64_t i = 0; i < group; ++i) amax = absmax_step(amax, v[i]);
       float a = fmaxf(amax, 1e-10f);
       float mult = 127.0f / a;
       for (int64_t i = 0; i < group; ++i) q[m * K + g * group + i] = i8_encode(v[i] * mult);

@@ -347,3 +347,20 @@ def test_row_padded_pins():
             assert scp.shape[1] == 16 and np.array_equal(scp[:, :10], sc[:, :10]) and not scp[:, 10:].any()
         else:
             assert scp.shape[0] == 16 and np.array_equal(scp[:10], sc) and not scp[10:].any()
+
+
+@pytest.mark.parametrize("pos", [0, 1, 63, 127])
+@pytest.mark.parametrize("nan_bits", [0x7F81, 0xFFC0, 0x7FC1])
+def test_absmax_skips_every_nan_wherever_it_sits(pos, nan_bits):
+    # signaling (0x7F81) or quiet NaN at any position: the scale is that of the group
+    # with the NaN replaced by 0, in both output formats, and the NaN encodes at +max
+    x = synth.to_bits(synth.quant_input(1, 128, seed=98))
+    y = x.copy()
+    y[0, pos] = nan_bits
+    x[0, pos] = 0
+    _, s_ref, _ = oracle.group_quant_canonical(x, 0, 128)
+    q, s, _ = oracle.group_quant_canonical(y, 0, 128)
+    assert s[0, 0] == s_ref[0, 0] and q[0, pos] == 0x7E
+    qi, si = oracle.group_quant_int8(y, 0, 128)
+    _, si_ref = oracle.group_quant_int8(x, 0, 128)
+    assert si[0, 0] == si_ref[0, 0] and qi[0, pos] == 127
