@@ -19,6 +19,7 @@ import torch
 __all__ = [
     "Fp8mmError", "lib", "per_token_group_quant_fp8", "per_token_group_quant_fp8_scatter",
     "fp8_scaled_mm", "silu_and_mul_masked_post_quant_fp8", "static_per_tensor_quant_fp8",
+    "per_token_group_quant_int8", "per_token_group_quant_fp8_row_padded",
     "requantize_with_max_scale_fp8", "masked_scale_shape", "get_device_status", "selftest_bounded_wait", "selftest_scale_math", "scale_shape", "scale_dtype",
     "alloc_group_quant_outputs", "SCALE_FP32", "SCALE_FP32_POW2", "SCALE_UE8M0_PACKED",
     "A_TENSOR", "A_ROW", "A_GROUP128", "A_GROUP128_COLMAJOR", "A_GROUP128_UE8M0", "B_TENSOR", "B_COL",
@@ -64,6 +65,10 @@ def lib():
         L.per_token_group_quant_fp8_scatter.restype = I
         L.silu_and_mul_masked_post_quant_fp8.argtypes = [P, I, P, I64, I64, I64, P, P, I, I, I, P]
         L.silu_and_mul_masked_post_quant_fp8.restype = I
+        L.per_token_group_quant_int8.argtypes = [P, I, P, P, I64, I64, I, I, I, P]
+        L.per_token_group_quant_int8.restype = I
+        L.per_token_group_quant_fp8_row_padded.argtypes = [P, I, P, P, I64, I64, I64, I, I, I, P]
+        L.per_token_group_quant_fp8_row_padded.restype = I
         L.static_per_tensor_quant_fp8.argtypes = [P, I, P, P, I64, P]
         L.static_per_tensor_quant_fp8.restype = I
         L.requantize_with_max_scale_fp8.argtypes = [P, P, P, P, I, I64, I64, P, P]
@@ -139,6 +144,27 @@ def per_token_group_quant_fp8(x, q, s, group: int, ue8m0: int = SCALE_FP32, scal
     st = lib().per_token_group_quant_fp8(_ptr(x), x_dtype, _ptr(q), _ptr(s), M, K, group, int(ue8m0),
                                          int(bool(scale_colmajor)), int(bool(fuse_silu_mul)), _stream(stream))
     _check(st, "per_token_group_quant_fp8")
+
+
+def per_token_group_quant_int8(x, q, s, group: int, scale_colmajor: bool = False, fuse_silu_mul: bool = False,
+                               stream=None):
+    """int8 group quant: x [M, K] (or [M, 2K] fused) -> q int8 [M, K], s fp32."""
+    M = x.shape[0]
+    K = x.shape[1] // 2 if fuse_silu_mul else x.shape[1]
+    st = lib().per_token_group_quant_int8(_ptr(x), _DTYPE_CODE[x.dtype], _ptr(q), _ptr(s), M, K, group,
+                                          int(bool(scale_colmajor)), int(bool(fuse_silu_mul)), _stream(stream))
+    _check(st, "per_token_group_quant_int8")
+
+
+def per_token_group_quant_fp8_row_padded(x, q, s, group: int, ue8m0: int = SCALE_FP32, scale_colmajor: bool = True,
+                                         stream=None):
+    """Group quant of x [M, K] into q [M_pad, K] / s sized for M_pad = q.shape[0]
+    rows; rows M .. M_pad-1 are zeroed."""
+    M, K = x.shape
+    st = lib().per_token_group_quant_fp8_row_padded(_ptr(x), _DTYPE_CODE[x.dtype], _ptr(q), _ptr(s), M, q.shape[0],
+                                                    K, group, int(ue8m0), int(bool(scale_colmajor)),
+                                                    _stream(stream))
+    _check(st, "per_token_group_quant_fp8_row_padded")
 
 
 def per_token_group_quant_fp8_scatter(x, dst_row, q, s, group: int, ue8m0: int = SCALE_UE8M0_PACKED,

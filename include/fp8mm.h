@@ -183,6 +183,34 @@ FP8MM_API int silu_and_mul_masked_post_quant_fp8(const void* x, int x_dtype, con
                                                  int scale_colmajor, fp8mm_stream_t stream);
 
 /*
+ * per_token_group_quant_int8
+ *   The int8 output format of the same group quant (sglang PR #33533,
+ *   "Verified": fp32 / ue8m0 / int8 formats; the entry-point notes name
+ *   sglang_per_token_group_quant_int8): per group, a = max(absmax, 1e-10),
+ *   s = fl32(a / 127), q = int8 of fl32(v * fl32(127 / a)) after min(., 127)
+ *   (NaN -> +127), rounded to nearest even, saturating at -128.
+ *   q      int8 [M, K], device, 16-byte aligned.
+ *   s      fp32, row-major [M, K/group] or column-major [K/group, pad4(M)].
+ *   Other arguments as per_token_group_quant_fp8 (no scatter, no masked layout).
+ */
+FP8MM_API int per_token_group_quant_int8(const void* x, int x_dtype, int8_t* q, float* s, int64_t M, int64_t K,
+                                         int group, int scale_colmajor, int fuse_silu_mul, fp8mm_stream_t stream);
+
+/*
+ * per_token_group_quant_fp8_row_padded
+ *   The group quant into outputs sized for M_pad >= M rows, rows M .. M_pad-1
+ *   zeroed (codes 0, scale entries 0): the row padding plus tail zeroing that
+ *   the plain entry cannot express (sglang PR #33533, entry-point dedup notes).
+ *   q  uint8 [M_pad, K].  s  as per_token_group_quant_fp8 with M_pad rows:
+ *   row-major [M_pad, cols] or column-major [cols, pad4(M_pad)], cols = K/group
+ *   (fp32) or ceil(K/group/4) (packed UE8M0).  Columns M_pad .. pad4(M_pad)-1
+ *   of a column-major buffer are not written.  Two launches on `stream`.
+ */
+FP8MM_API int per_token_group_quant_fp8_row_padded(const void* x, int x_dtype, uint8_t* q, void* s, int64_t M,
+                                                   int64_t M_pad, int64_t K, int group, int ue8m0,
+                                                   int scale_colmajor, fp8mm_stream_t stream);
+
+/*
  * static_per_tensor_quant_fp8
  *   Static per-tensor activation quant with a given scale (the checkpoint's
  *   activation scale, prhub summary of sglang PR #33148, Key source snippets):

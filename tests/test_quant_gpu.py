@@ -111,6 +111,17 @@ def test_encode_every_16bit_value(dtype):
     _compare(x, dtype, 128, 0, False, False)
 
 
+@pytest.mark.parametrize("dtype", [0, 1])
+def test_every_16bit_pattern_with_non_finite(dtype):
+    # all 65536 bit patterns, signaling and quiet NaN and infinities included, in
+    # their natural order (so whole groups of NaN and inf next to finite groups)
+    vals = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    for fmt, cm in ((0, False), (2, True)):
+        _compare(synth.from_bits(vals.reshape(512, 128), DT[dtype]), dtype, 128, fmt, cm, False)
+    _compare(synth.from_bits(vals.reshape(1024, 64), DT[dtype]), dtype, 32, 1, True, False)
+    _compare(synth.from_bits(vals.reshape(64, 1024), DT[dtype]), dtype, 1024, 0, False, False)
+
+
 def test_scatter_topk8_of_256():
     dev = require_gpu()
     M, K = 512, 7168
