@@ -236,6 +236,10 @@ def run_gpu(args, rank, world, local_rank):
     if rank == 0:
         quant_obj = bench_group_quant(torch, fm, synth, dev, flush)
 
+    widened = None
+    if rank == 0:
+        widened = bench_widened(torch, fm, synth, dev, flush, work[0])
+
     # ---- end to end through the C ABI with host buffers
     e2e = None
     if rank == 0 and not args.no_e2e:
@@ -243,7 +247,7 @@ def run_gpu(args, rank, world, local_rank):
 
     res = dict(step_ms=tot_step_ms / args.steps, gemm_ms=tot_gemm_ms / args.steps,
                quant_ms=tot_quant_ms / args.steps, wall=wall, step_flops=step_flops,
-               step_quant_bytes=step_quant_bytes, clocks=clocks, quant=quant_obj, e2e=e2e,
+               step_quant_bytes=step_quant_bytes, clocks=clocks, quant=quant_obj, e2e=e2e, widened=widened,
                per_shape_gemm_ms=[x / args.steps for x in per_shape_gemm], launches=2 * len(work) * args.steps)
     return res
 
@@ -297,6 +301,71 @@ def bench_group_quant(torch, fm, synth, dev, flush, reps=20):
     return out
 
 
+def _median_us(torch, flush, fn, reps):
+    for _ in range(3):
+        fn()
+    ts = []
+    for _ in range(reps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        ts.append((a, b))
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in ts) * 1e3
+
+
+def bench_widened(torch, fm, synth, dev, flush, w0, reps=10):
+    """The paths beyond the headline step, each alone on one workload:
+    block-scaled GEMM (A 1x128 UE8M0 group scales x B 128x128 block scales) on the
+    first prefill shape, and the HBM-bound quant variants on M=8192, K=7168."""
+    out = {}
+    M, K, N = w0["M"], w0["K"], w0["N"]
+    words = fm.scale_shape(M, K, 128, fm.SCALE_UE8M0_PACKED, True)
+    a_w = torch.empty(words, dtype=torch.int32, device=dev)
+    A = torch.empty((M, K), dtype=torch.uint8, device=dev)
+    fm.per_token_group_quant_fp8(w0["X"], A, a_w, 128, fm.SCALE_UE8M0_PACKED, True)
+    b_blk = torch.rand(((N + 127) // 128, K // 128), generator=torch.Generator(device=dev).manual_seed(7),
+                       device=dev) * 1e-3 + 1e-4
+    us = _median_us(torch, flush, lambda: fm.fp8_scaled_mm(A, w0["B"], a_w, b_blk, fm.A_GROUP128_UE8M0 | fm.B_BLOCK128,
+                                                           w0["D"]), reps)
+    out["block_scaled_gemm"] = {"workload": f"{M}x{K}x{N}, A group-128 UE8M0 (packed, column-major) x B 128x128 fp32",
+                                "us": round(us, 1), "tflops": round(flops(M, K, N) / (us * 1e-6) / 1e12, 1)}
+    del A, a_w
+    QM, QK = QUANT_M, QUANT_K
+    x = synth.quant_input(QM, QK, torch.bfloat16, seed=8, device=dev)
+    q = torch.empty((QM, QK), dtype=torch.uint8, device=dev)
+    sc = torch.full((1,), 0.01, dtype=torch.float32, device=dev)
+    us = _median_us(torch, flush, lambda: fm.static_per_tensor_quant_fp8(x, sc, q), reps)
+    out["static_per_tensor_quant"] = {"workload": f"{QM}x{QK} bf16", "us": round(us, 2), "bytes": QM * QK * 3}
+    qi = q.view(torch.int8)
+    si = torch.empty(fm.scale_shape(QM, QK, 128, fm.SCALE_FP32, True), dtype=torch.float32, device=dev)
+    us = _median_us(torch, flush, lambda: fm.per_token_group_quant_int8(x, qi, si, 128, True), reps)
+    out["int8_group_quant"] = {"workload": f"{QM}x{QK} bf16, group 128, fp32 column-major scales",
+                               "us": round(us, 2), "bytes": QM * QK * 3 + si.numel() * 4}
+    MP = QM
+    xs = x[: QM - 192]
+    sp = torch.empty(fm.scale_shape(MP, QK, 128, fm.SCALE_FP32, True), dtype=torch.float32, device=dev)
+    us = _median_us(torch, flush, lambda: fm.per_token_group_quant_fp8_row_padded(xs, q, sp, 128), reps)
+    out["row_padded_group_quant"] = {"workload": f"M={QM - 192} padded to {MP}, K={QK} bf16, group 128, fp32 "
+                                                 "column-major scales", "us": round(us, 2),
+                                     "bytes": (QM - 192) * QK * 2 + MP * QK + sp.numel() * 4}
+    del x, xs, q, sp, si
+    NW, KW = 2 * 14336, 4096
+    w = torch.randint(0, 126, (NW, KW), generator=torch.Generator(device=dev).manual_seed(9), dtype=torch.uint8,
+                      device=dev)
+    w_out = torch.empty_like(w)
+    ss = torch.tensor([0.011, 0.013], dtype=torch.float32, device=dev)
+    us = _median_us(torch, flush, lambda: fm.requantize_with_max_scale_fp8(w, ss, [14336, 14336], w_out=w_out), reps)
+    out["requantize_with_max_scale"] = {"workload": f"gate/up weight {NW}x{KW}, 2 shards", "us": round(us, 2),
+                                        "bytes": NW * KW * 2}
+    for v in out.values():
+        if "bytes" in v:
+            v["gbs"] = round(v["bytes"] / (v["us"] * 1e-6) / 1e9, 1)
+    return out
+
+
 def bench_e2e(torch, fm, work, flush, args):
     """Same step through the C ABI from pinned host buffers: H2D of each
     activation, quant + GEMM, D2H of each output, all inside the timed region."""
@@ -336,14 +405,15 @@ def bench_e2e(torch, fm, work, flush, args):
 def run_kernel_case(args):
     """Launch one kernel on its workload warmup + steps times (for profilers)
     and print its event-timed median.  gemm: a prefill shape (--shape, default
-    8320x5376x21504) or --mnk M,K,N, rowwise scales; quant / quant_fused:
+    8320x5376x21504) or --mnk M,K,N, rowwise scales; gemm_block: the same
+    shapes with group-128 UE8M0 A scales and 128x128 B block scales; quant / quant_fused:
     group-128 quant of M=8192, K=7168 bf16 with UE8M0 packed column-major
     scales."""
     import torch
     import fp8_scaled_gemm_mm_gb300 as fm
     from fp8_scaled_gemm_mm_gb300 import synth
     dev = torch.device("cuda", 0)
-    if args.kernel_case == "gemm":
+    if args.kernel_case in ("gemm", "gemm_block"):
         M, K, N = SHAPES[args.shape] if not args.mnk else tuple(int(v) for v in args.mnk.split(","))
         X = synth.normal((M, K), 1.0, seed=1, device=dev)
         W = synth.normal((N, K), 0.02, seed=2, device=dev)
@@ -359,6 +429,17 @@ def run_kernel_case(args):
 
         def launch():
             fm.fp8_scaled_mm(A, B, a_s, b_s, fm.A_ROW | fm.B_COL, D)
+
+        if args.kernel_case == "gemm_block":
+            a_s = torch.empty(fm.scale_shape(M, K, 128, fm.SCALE_UE8M0_PACKED, True), dtype=torch.int32, device=dev)
+            X = synth.normal((M, K), 1.0, seed=1, device=dev)
+            fm.per_token_group_quant_fp8(X, A, a_s, 128, fm.SCALE_UE8M0_PACKED, True)
+            del X
+            b_s = torch.rand(((N + 127) // 128, K // 128), generator=torch.Generator(device=dev).manual_seed(7),
+                             device=dev) * 1e-3 + 1e-4
+
+            def launch():
+                fm.fp8_scaled_mm(A, B, a_s, b_s, fm.A_GROUP128_UE8M0 | fm.B_BLOCK128, D)
     else:
         fuse = args.kernel_case == "quant_fused"
         M, K = QUANT_M, QUANT_K
@@ -379,9 +460,10 @@ def run_kernel_case(args):
         ts.append((a, b))
     torch.cuda.synchronize()
     us = statistics.median(a.elapsed_time(b) for a, b in ts) * 1e3
-    rate = work / (us * 1e-6) / (1e12 if args.kernel_case == "gemm" else 1e9)
+    is_gemm = args.kernel_case.startswith("gemm")
+    rate = work / (us * 1e-6) / (1e12 if is_gemm else 1e9)
     print(json.dumps({"kernel_case": args.kernel_case, "us": round(us, 2),
-                      ("tflops" if args.kernel_case == "gemm" else "gbs"): round(rate, 1)}), flush=True)
+                      ("tflops" if is_gemm else "gbs"): round(rate, 1)}), flush=True)
     return 0
 
 
@@ -461,7 +543,7 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=16, help="oracle rows per shape per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--kernel-case", choices=["gemm", "quant", "quant_fused"], default=None,
+    ap.add_argument("--kernel-case", choices=["gemm", "gemm_block", "quant", "quant_fused"], default=None,
                     help="run a single kernel on its workload (for profilers) instead of the benchmark")
     ap.add_argument("--shape", type=int, default=0, help="prefill shape index for --kernel-case gemm")
     ap.add_argument("--mnk", default=None, help="M,K,N for --kernel-case gemm instead of a prefill shape")
@@ -546,6 +628,14 @@ def main():
         line["group_quant"]["plain"]["traffic"] = load_traffic("group_quant", qhash)
         line["group_quant"]["fused_silu_mul"]["traffic"] = load_traffic("group_quant", qhash,
                                                                         "fused_bytes_per_launch")
+    if res["widened"]:
+        wd = res["widened"]
+        for k, v in wd.items():
+            if "gbs" in v:
+                v["frac_hbm"] = round(v["gbs"] / hbm_peak, 4)
+            if "tflops" in v:
+                v["frac_fp8_peak"] = round(v["tflops"] / fp8_peak, 4)
+        line["widened"] = wd
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_rows)
     print(json.dumps(line), flush=True)

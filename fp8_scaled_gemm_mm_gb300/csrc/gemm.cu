@@ -19,9 +19,10 @@
 // from K so that a group's A panel stays in L2) so that the CTAs running at the
 // same time share A and B panels in L2.
 //
-// Per-group A scales (one per 128-wide K block, the layout the group quant produces):
-// every K block goes to its own TMEM accumulator and the epilogue promotes it,
-// acc += a_s[m, kb] * partial_kb, in fp32 registers.
+// Per-group A scales (one per 128-wide K block, the layout the group quant produces),
+// optionally with 128 x 128 block B scales, run in fp8_gemm_group_kernel: every K
+// block goes to its own TMEM accumulator (a ring of four) and eight epilogue warps
+// promote it, acc += a_s[m, kb] (* b_s[n/128, kb]) * partial_kb, in fp32 registers.
 //
 // Deterministic mode uses one tile shape (BM=128, BN=64, BK=128), one instruction
 // shape and the natural K-block order for every problem, with no split of K, so row
@@ -189,7 +190,7 @@ __device__ __forceinline__ bool store_block(const CUtensorMap* tmD, uint8_t* buf
   return true;
 }
 
-template <int BN, int STAGES, bool GROUP_A>
+template <int BN, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmD, const GemmArgs p) {
@@ -275,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = blockIdx.x; ok && t < p.tiles; t += gridDim.x) {
         for (int kb = 0; ok && kb < p.num_kb; ++kb) {
           const uint32_t acc = acc_i & 1u;
-          if (GROUP_A || kb == 0) {
+          if (kb == 0) {
             ok = mbar_wait(&tempty[acc], ((acc_i >> 1) & 1u) ^ 1u, abort_flag, p.status, p.timeout_ns);
             if (!ok) break;
             tc_fence_after();
@@ -288,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t bdesc = smem_desc_sw128(smem_u32(smem + L::OFF_B + stage * L::B_BYTES));
 #pragma unroll
           for (int k = 0; k < BK / UMMA_K; ++k) {
-            const uint32_t accumulate = (GROUP_A ? k : (kb | k)) != 0 ? 1u : 0u;
+            const uint32_t accumulate = (kb | k) != 0 ? 1u : 0u;
             mma_f8f6f4(d, adesc + static_cast<uint64_t>(k * UMMA_K / 16),
                        bdesc + static_cast<uint64_t>(k * UMMA_K / 16), idesc, accumulate);
           }
@@ -297,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             stage = 0;
             phase ^= 1u;
           }
-          if (GROUP_A || kb == p.num_kb - 1) {
+          if (kb == p.num_kb - 1) {
             mma_commit(&tfull[acc]);
             ++acc_i;
           }
@@ -322,72 +323,319 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row = mb * BM + q * 32 + lane;
       const int r0 = mb * BM + q * 32;
       const int nbase = nb * BN;
-      if constexpr (!GROUP_A) {
-        const uint32_t acc = acc_i & 1u;
-        if (!mbar_wait(&tfull[acc], (acc_i >> 1) & 1u, abort_flag, p.status, p.timeout_ns)) break;
-        tc_fence_after();
-        const float sa = a_scale_at(p, row, 0);
+      const uint32_t acc = acc_i & 1u;
+      if (!mbar_wait(&tfull[acc], (acc_i >> 1) & 1u, abort_flag, p.status, p.timeout_ns)) break;
+      tc_fence_after();
+      const float sa = a_scale_at(p, row, 0);
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(lane_addr + acc * BN + c * 32, r);
-          tmem_ld_wait();
-          if (c == BN / 32 - 1) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty[acc]);
-          }
-          float sb[32], bs[32];
-          load_col_vectors(p, nbase + c * 32, sb, bs);
-          uint32_t w[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float v0 = __uint_as_float(r[2 * j]) * sa * sb[2 * j] + bs[2 * j];
-            const float v1 = __uint_as_float(r[2 * j + 1]) * sa * sb[2 * j + 1] + bs[2 * j + 1];
-            w[j] = pack2(v0, v1, p.out_fp16);
-          }
-          if (store_block(&tmD, stage_buf + dbuf * L::D_BYTES, w, lane, nbase + c * 32, r0, p.M, p.N)) dbuf ^= 1;
-        }
-        ++acc_i;
-      } else {
-        float accum[BN];
-#pragma unroll
-        for (int j = 0; j < BN; ++j) accum[j] = 0.0f;
-        bool ok = true;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
-          const uint32_t acc = acc_i & 1u;
-          ok = mbar_wait(&tfull[acc], (acc_i >> 1) & 1u, abort_flag, p.status, p.timeout_ns);
-          if (!ok) break;
-          tc_fence_after();
-          float sa = a_scale_at(p, row, kb);
-          if (p.b_mode == 2) sa *= b_block_scale_at(p, nbase, kb);
-#pragma unroll
-          for (int c = 0; c < BN / 32; ++c) {
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(lane_addr + acc * BN + c * 32, r);
-            tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) accum[c * 32 + j] = fmaf(sa, __uint_as_float(r[j]), accum[c * 32 + j]);
-          }
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(lane_addr + acc * BN + c * 32, r);
+        tmem_ld_wait();
+        if (c == BN / 32 - 1) {
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&tempty[acc]);
-          ++acc_i;
         }
-        if (!ok) break;
+        float sb[32], bs[32];
+        load_col_vectors(p, nbase + c * 32, sb, bs);
+        uint32_t w[16];
 #pragma unroll
-        for (int c = 0; c < BN / 32; ++c) {
-          float sb[32], bs[32];
-          load_col_vectors(p, nbase + c * 32, sb, bs);
-          uint32_t w[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float v0 = accum[c * 32 + 2 * j] * sb[2 * j] + bs[2 * j];
-            const float v1 = accum[c * 32 + 2 * j + 1] * sb[2 * j + 1] + bs[2 * j + 1];
-            w[j] = pack2(v0, v1, p.out_fp16);
+        for (int j = 0; j < 16; ++j) {
+          const float v0 = __uint_as_float(r[2 * j]) * sa * sb[2 * j] + bs[2 * j];
+          const float v1 = __uint_as_float(r[2 * j + 1]) * sa * sb[2 * j + 1] + bs[2 * j + 1];
+          w[j] = pack2(v0, v1, p.out_fp16);
+        }
+        if (store_block(&tmD, stage_buf + dbuf * L::D_BYTES, w, lane, nbase + c * 32, r0, p.M, p.N)) dbuf ^= 1;
+      }
+      ++acc_i;
+    }
+    if (lane == 0) bulk_wait<0>();
+    __syncwarp();
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, L::TMEM_COLS);
+  }
+}
+
+// ------------------------------------- per-group A (and block B) scales
+//
+// The MMA cannot apply a scale that changes along K, so every 128-wide K block
+// accumulates into its own TMEM buffer (a ring of NACC) and the epilogue folds it in:
+// acc[m, n] += a_s[m, kb] * b_s[n / 128, kb] * partial_kb[m, n] (b_s = 1 without
+// block scales).  Eight epilogue warps share the work: warp w reads TMEM lane
+// quarter w % 4 (the only one it may access) and one half of the BN columns.  The
+// buffer is handed back to the MMA warp as soon as its values are in registers.
+
+constexpr int kGroupEpiWarps = 8;
+constexpr int kGroupThreads = 64 + 32 * kGroupEpiWarps;
+
+template <int BN, int STAGES, int NACC>
+struct GroupLayout {
+  static constexpr int A_BYTES = BM * BK;
+  static constexpr int B_BYTES = BN * BK;
+  static constexpr int D_BYTES = 32 * 64;
+  static constexpr int OFF_A = 0;
+  static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+  static constexpr int OFF_D = OFF_B + STAGES * B_BYTES;
+  static constexpr int OFF_BAR = OFF_D + kGroupEpiWarps * 2 * D_BYTES;
+  static constexpr int NBARS = 2 * STAGES + 2 * NACC + 1;
+  static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
+  static constexpr int BYTES = OFF_MISC + 16;
+  static constexpr int ALLOC = BYTES + 1024;
+  static constexpr uint32_t TMEM_COLS = pow2_at_least(NACC * BN);
+  static_assert(BN == 128, "block B scales need one 128-column block per tile");
+  static_assert(NACC * BN <= 512, "TMEM columns");
+  static_assert(ALLOC <= 232448, "shared memory budget");
+};
+
+// The scales of K block kb are fetched kScalePrefetch blocks ahead as raw words and
+// decoded when used, so no arithmetic waits on the load.
+constexpr int kScalePrefetch = 4;
+
+// Scale stream of one epilogue thread for the K blocks of a tile: A scale words of
+// its row (AMODE fixes the layout at compile time) and, with BBLOCK, the block B
+// scale of the tile's 128 columns.  Rows past M read row M-1 and K blocks past the
+// end read the last one; neither value is used.
+template <int AMODE, bool BBLOCK>
+struct ScaleStream {
+  const uint32_t* a;
+  int64_t a_step;   // words between consecutive K blocks (UE8M0: between groups of four)
+  const float* b;
+  int last;         // num_kb - 1
+  __device__ __forceinline__ ScaleStream(const GemmArgs& p, int row, int nbase) {
+    const int r = row < p.M ? row : p.M - 1;
+    const uint32_t* base = reinterpret_cast<const uint32_t*>(p.a_scale);
+    if (AMODE == FP8MM_SCALE_A_GROUP128) {
+      a = base + static_cast<int64_t>(r) * p.a_ld;
+      a_step = 1;
+    } else {
+      a = base + r;
+      a_step = p.a_ld;
+    }
+    b = p.b_scale + static_cast<int64_t>(nbase >> 7) * p.b_ld;
+    last = p.num_kb - 1;
+  }
+  __device__ __forceinline__ uint32_t a_raw(int kb) const {
+    kb = kb < last ? kb : last;
+    return __ldg(a + (AMODE == FP8MM_SCALE_A_GROUP128_UE8M0 ? (kb >> 2) : kb) * a_step);
+  }
+  __device__ __forceinline__ float b_raw(int kb) const {
+    if (!BBLOCK) return 1.0f;
+    kb = kb < last ? kb : last;
+    return __ldg(b + kb);
+  }
+  __device__ __forceinline__ static float decode(uint32_t raw, int kb) {
+    if (AMODE == FP8MM_SCALE_A_GROUP128_UE8M0) return __uint_as_float(((raw >> (8 * (kb & 3))) & 0xFFu) << 23);
+    return __uint_as_float(raw);
+  }
+};
+
+// Packed fp32 pairs: fma.rn.f32x2 performs two IEEE fused multiply-adds.
+typedef unsigned long long f32x2_t;
+__device__ __forceinline__ f32x2_t pack_f2(uint32_t lo, uint32_t hi) {
+  f32x2_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+  return r;
+}
+__device__ __forceinline__ f32x2_t fma_f2(f32x2_t a, f32x2_t b, f32x2_t c) {
+  f32x2_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ void unpack_f2(f32x2_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+template <int BN, int STAGES, int NACC, int AMODE, bool BBLOCK>
+__global__ void __launch_bounds__(kGroupThreads, 1)
+    fp8_gemm_group_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                          const __grid_constant__ CUtensorMap tmD, const GemmArgs p) {
+  using L = GroupLayout<BN, STAGES, NACC>;
+  constexpr int HALF = BN / 2;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + NACC;
+  uint64_t* drain = tempty + NACC;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmD);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int i = 0; i < NACC; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], kGroupEpiWarps);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, L::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------- producer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      int64_t issued = 0;
+      for (int t = blockIdx.x; t < p.tiles && !*abort_flag; t += gridDim.x) {
+        int mb, nb;
+        tile_coords(p, t, mb, nb);
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status, p.timeout_ns)) break;
+          mbar_arrive_expect_tx(&full[stage], L::A_BYTES + L::B_BYTES);
+          tma_load_2d(&tmA, &full[stage], smem + L::OFF_A + stage * L::A_BYTES, kb * BK, mb * BM);
+          tma_load_2d(&tmB, &full[stage], smem + L::OFF_B + stage * L::B_BYTES, kb * BK, nb * BN);
+          ++issued;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
           }
-          if (store_block(&tmD, stage_buf + dbuf * L::D_BYTES, w, lane, nbase + c * 32, r0, p.M, p.N)) dbuf ^= 1;
         }
+      }
+      const int outstanding = static_cast<int>(issued < STAGES ? issued : STAGES);
+      for (int j = 1; j <= outstanding; ++j) {
+        int s = static_cast<int>(stage) - j;
+        uint32_t ph = phase;
+        if (s < 0) {
+          s += STAGES;
+          ph ^= 1u;
+        }
+        volatile int never = 0;
+        mbar_wait(&full[s], ph, &never, p.status, p.timeout_ns);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issue
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
+      uint32_t stage = 0, phase = 0, acc_i = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < p.tiles; t += gridDim.x) {
+        for (int kb = 0; ok && kb < p.num_kb; ++kb) {
+          const uint32_t acc = acc_i % NACC;
+          ok = mbar_wait(&tempty[acc], ((acc_i / NACC) & 1u) ^ 1u, abort_flag, p.status, p.timeout_ns);
+          if (!ok) break;
+          tc_fence_after();
+          ok = mbar_wait(&full[stage], phase, abort_flag, p.status, p.timeout_ns);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t d = tmem_base + acc * BN;
+          const uint64_t adesc = smem_desc_sw128(smem_u32(smem + L::OFF_A + stage * L::A_BYTES));
+          const uint64_t bdesc = smem_desc_sw128(smem_u32(smem + L::OFF_B + stage * L::B_BYTES));
+#pragma unroll
+          for (int k = 0; k < BK / UMMA_K; ++k)
+            mma_f8f6f4(d, adesc + static_cast<uint64_t>(k * UMMA_K / 16),
+                       bdesc + static_cast<uint64_t>(k * UMMA_K / 16), idesc, k != 0 ? 1u : 0u);
+          mma_commit(&empty[stage]);
+          mma_commit(&tfull[acc]);
+          ++acc_i;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      mma_commit(drain);
+      volatile int never = 0;
+      mbar_wait(drain, 0, &never, p.status, p.timeout_ns);
+    }
+  } else {
+    // ------------------------------------------------------------- epilogue
+    const int ew = warp - 2;
+    const int q = warp & 3;                   // TMEM lane quarter this warp may access
+    const int h = ew >> 2;                    // column half
+    uint8_t* stage_buf = smem + L::OFF_D + ew * 2 * L::D_BYTES;
+    int dbuf = 0;
+    uint32_t acc_i = 0;
+    const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + h * HALF;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < p.tiles; t += gridDim.x) {
+      int mb, nb;
+      tile_coords(p, t, mb, nb);
+      const int row = mb * BM + q * 32 + lane;
+      const int r0 = mb * BM + q * 32;
+      const int nbase = nb * BN;
+      f32x2_t accum[HALF / 2];
+#pragma unroll
+      for (int j = 0; j < HALF / 2; ++j) accum[j] = 0ull;
+      const ScaleStream<AMODE, BBLOCK> ss(p, row, nbase);
+      uint32_t ra[kScalePrefetch];
+      float rb[kScalePrefetch];
+#pragma unroll
+      for (int i = 0; i < kScalePrefetch; ++i) {
+        ra[i] = ss.a_raw(i);
+        rb[i] = ss.b_raw(i);
+      }
+#pragma unroll 4
+      for (int kb = 0; kb < p.num_kb; ++kb) {
+        const uint32_t a_raw = ra[0];
+        const float b_raw = rb[0];
+#pragma unroll
+        for (int i = 0; i + 1 < kScalePrefetch; ++i) {
+          ra[i] = ra[i + 1];
+          rb[i] = rb[i + 1];
+        }
+        ra[kScalePrefetch - 1] = ss.a_raw(kb + kScalePrefetch);
+        rb[kScalePrefetch - 1] = ss.b_raw(kb + kScalePrefetch);
+        const uint32_t acc = acc_i % NACC;
+        ok = mbar_wait(&tfull[acc], (acc_i / NACC) & 1u, abort_flag, p.status, p.timeout_ns);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t r0v[32], r1v[32];
+        tmem_ld_32x32b_x32(lane_addr + acc * BN, r0v);
+        tmem_ld_32x32b_x32(lane_addr + acc * BN + 32, r1v);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
+        const float sk = ScaleStream<AMODE, BBLOCK>::decode(a_raw, kb) * b_raw;
+        const f32x2_t sk2 = pack_f2(__float_as_uint(sk), __float_as_uint(sk));
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          accum[j] = fma_f2(sk2, pack_f2(r0v[2 * j], r0v[2 * j + 1]), accum[j]);
+          accum[16 + j] = fma_f2(sk2, pack_f2(r1v[2 * j], r1v[2 * j + 1]), accum[16 + j]);
+        }
+        ++acc_i;
+      }
+      if (!ok) break;
+#pragma unroll
+      for (int c = 0; c < HALF / 32; ++c) {
+        const int n0 = nbase + h * HALF + c * 32;
+        float sb[32], bs[32];
+        load_col_vectors(p, n0, sb, bs);
+        uint32_t w[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          float a0, a1;
+          unpack_f2(accum[c * 16 + j], a0, a1);
+          const float v0 = a0 * sb[2 * j] + bs[2 * j];
+          const float v1 = a1 * sb[2 * j + 1] + bs[2 * j + 1];
+          w[j] = pack2(v0, v1, p.out_fp16);
+        }
+        if (store_block(&tmD, stage_buf + dbuf * L::D_BYTES, w, lane, n0, r0, p.M, p.N)) dbuf ^= 1;
       }
     }
     if (lane == 0) bulk_wait<0>();
@@ -611,11 +859,11 @@ struct Config {
   bool group_a;
 };
 
-template <int BN, int STAGES, bool GROUP_A>
+template <int BN, int STAGES>
 cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td, const GemmArgs& p,
                    int grid, cudaStream_t st) {
   using L = Layout<BN, STAGES>;
-  auto kern = fp8_gemm_kernel<BN, STAGES, GROUP_A>;
+  auto kern = fp8_gemm_kernel<BN, STAGES>;
   static int configured_dev = -1;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -626,6 +874,42 @@ cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorM
   }
   kern<<<grid, kThreads, L::ALLOC, st>>>(ta, tb, td, p);
   return cudaGetLastError();
+}
+
+constexpr int kGroupBN = 128, kGroupStages = 6, kGroupAcc = 4;
+
+template <int AMODE, bool BBLOCK>
+cudaError_t launch_group(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td, const GemmArgs& p,
+                         int grid, cudaStream_t st) {
+  using L = GroupLayout<kGroupBN, kGroupStages, kGroupAcc>;
+  auto kern = fp8_gemm_group_kernel<kGroupBN, kGroupStages, kGroupAcc, AMODE, BBLOCK>;
+  static int configured_dev = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_dev != dev) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
+    if (e != cudaSuccess) return e;
+    configured_dev = dev;
+  }
+  kern<<<grid, kGroupThreads, L::ALLOC, st>>>(ta, tb, td, p);
+  return cudaGetLastError();
+}
+
+template <bool BBLOCK>
+cudaError_t launch_group_a(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td, const GemmArgs& p,
+                           int grid, cudaStream_t st) {
+  switch (p.a_mode) {
+    case FP8MM_SCALE_A_GROUP128: return launch_group<FP8MM_SCALE_A_GROUP128, BBLOCK>(ta, tb, td, p, grid, st);
+    case FP8MM_SCALE_A_GROUP128_COLMAJOR:
+      return launch_group<FP8MM_SCALE_A_GROUP128_COLMAJOR, BBLOCK>(ta, tb, td, p, grid, st);
+    default: return launch_group<FP8MM_SCALE_A_GROUP128_UE8M0, BBLOCK>(ta, tb, td, p, grid, st);
+  }
+}
+
+cudaError_t launch_group_modes(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td,
+                               const GemmArgs& p, int grid, cudaStream_t st) {
+  return p.b_mode == 2 ? launch_group_a<true>(ta, tb, td, p, grid, st)
+                       : launch_group_a<false>(ta, tb, td, p, grid, st);
 }
 
 int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
@@ -673,7 +957,7 @@ int pick_splits(int64_t M, int64_t N, int num_kb, int sms) {
 // Shape-keyed tile table.  Deterministic mode picks its tile from N alone, so every M
 // (and every prefix / suffix of the rows) runs the same tile, K order and instruction.
 Config pick_config(int64_t M, int64_t N, bool deterministic, bool group_a, int sms) {
-  if (group_a) return {64, 8, true};
+  if (group_a) return {kGroupBN, kGroupStages, true};
   if (deterministic) {
     if (N >= 1024) return {256, 4, false};
     if (N >= 256) return {128, 6, false};
@@ -791,12 +1075,12 @@ extern "C" int fp8_scaled_mm(const void* A, const void* B, const float* a_scale,
   const int grid = p.tiles < sms ? p.tiles : sms;
   cudaError_t e;
   if (cfg.group_a)
-    e = launch<64, 8, true>(ta, tb, td, p, grid, st);
+    e = launch_group_modes(ta, tb, td, p, grid, st);
   else if (cfg.bn == 256)
-    e = launch<256, 4, false>(ta, tb, td, p, grid, st);
+    e = launch<256, 4>(ta, tb, td, p, grid, st);
   else if (cfg.bn == 128)
-    e = launch<128, 6, false>(ta, tb, td, p, grid, st);
+    e = launch<128, 6>(ta, tb, td, p, grid, st);
   else
-    e = launch<64, 8, false>(ta, tb, td, p, grid, st);
+    e = launch<64, 8>(ta, tb, td, p, grid, st);
   return e == cudaSuccess ? FP8MM_OK : FP8MM_ECUDA;
 }
