@@ -367,28 +367,44 @@ __global__ void __launch_bounds__(kThreads, 1)
 // The MMA cannot apply a scale that changes along K, so every 128-wide K block
 // accumulates into its own TMEM buffer (a ring of NACC) and the epilogue folds it in:
 // acc[m, n] += a_s[m, kb] * b_s[n / 128, kb] * partial_kb[m, n] (b_s = 1 without
-// block scales).  Eight epilogue warps share the work: warp w reads TMEM lane
-// quarter w % 4 (the only one it may access) and one half of the BN columns.  The
-// buffer is handed back to the MMA warp as soon as its values are in registers.
+// block scales).  4 x SPLIT epilogue warps share the work: warp w reads TMEM lane
+// quarter w % 4 (the only one it may access) and one of SPLIT column slices of the
+// tile, holding its slice of acc in fp32 registers.  The buffer is handed back to the
+// MMA warp as soon as its values are in registers.
+//
+// Tile width matters more than anything else here: with M = 128, MMAs of N = 128
+// reach about 60 % of the tensor rate on this part and N = 256 about 95 %.  So the
+// preferred form is 128 x 256 with two accumulators (all 512 TMEM columns) and
+// SPLIT = 2, which needs 128 accumulator registers per epilogue thread: warpgroup 0
+// (TMA and MMA threads) gives its registers to the two epilogue warpgroups with
+// setmaxnreg (40 / 232 of the 168 per thread the block is launched with; an SM
+// sub-partition holds 16K registers and here three warps).  Without that split the
+// form is 128 x 192, SPLIT = 3, 128 registers a thread.  Plain fp32 FMAs: the packed
+// f32x2 form needs register pairs the TMEM loads do not produce, and the moves cost
+// more than the packing saves.
 
-constexpr int kGroupEpiWarps = 8;
-constexpr int kGroupThreads = 64 + 32 * kGroupEpiWarps;
-
-template <int BN, int STAGES, int NACC>
+template <int BN, int STAGES, int NACC, int SPLIT, bool RS>
 struct GroupLayout {
+  static constexpr int EPI_WARPS = 4 * SPLIT;
+  static constexpr int FIRST_EPI = RS ? 4 : 2;   // with a register split, warpgroup 0 is TMA + MMA
+  static constexpr int THREADS = 32 * FIRST_EPI + 32 * EPI_WARPS;
+  static constexpr int REG_LO = 40, REG_HI = 232;   // setmaxnreg values of warpgroup 0 / the others
+  static constexpr int WCOLS = BN / SPLIT;   // columns of one epilogue warp
   static constexpr int A_BYTES = BM * BK;
   static constexpr int B_BYTES = BN * BK;
   static constexpr int D_BYTES = 32 * 64;
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
   static constexpr int OFF_D = OFF_B + STAGES * B_BYTES;
-  static constexpr int OFF_BAR = OFF_D + kGroupEpiWarps * 2 * D_BYTES;
+  static constexpr int OFF_BAR = OFF_D + EPI_WARPS * 2 * D_BYTES;
   static constexpr int NBARS = 2 * STAGES + 2 * NACC + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
   static constexpr int BYTES = OFF_MISC + 16;
   static constexpr int ALLOC = BYTES + 1024;
   static constexpr uint32_t TMEM_COLS = pow2_at_least(NACC * BN);
-  static_assert(BN == 128, "block B scales need one 128-column block per tile");
+  static_assert(WCOLS % 32 == 0 && WCOLS <= 128 && 128 % WCOLS == 0,
+                "each epilogue warp's columns must lie in one 128-column block");
+  static_assert((BN * BK) % 1024 == 0, "B stage must keep 1024-byte alignment");
   static_assert(NACC * BN <= 512, "TMEM columns");
   static_assert(ALLOC <= 232448, "shared memory budget");
 };
@@ -435,28 +451,22 @@ struct ScaleStream {
   }
 };
 
-// Packed fp32 pairs: fma.rn.f32x2 performs two IEEE fused multiply-adds.
-typedef unsigned long long f32x2_t;
-__device__ __forceinline__ f32x2_t pack_f2(uint32_t lo, uint32_t hi) {
-  f32x2_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
-  return r;
+// Per-warpgroup register budgets (setmaxnreg; all four warps of the warpgroup execute it).
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
-__device__ __forceinline__ f32x2_t fma_f2(f32x2_t a, f32x2_t b, f32x2_t c) {
-  f32x2_t r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-  return r;
-}
-__device__ __forceinline__ void unpack_f2(f32x2_t v, float& lo, float& hi) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
-template <int BN, int STAGES, int NACC, int AMODE, bool BBLOCK>
-__global__ void __launch_bounds__(kGroupThreads, 1)
+template <int BN, int STAGES, int NACC, int SPLIT, bool RS, int AMODE, bool BBLOCK>
+__global__ void __launch_bounds__(GroupLayout<BN, STAGES, NACC, SPLIT, RS>::THREADS, 1)
     fp8_gemm_group_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                           const __grid_constant__ CUtensorMap tmD, const GemmArgs p) {
-  using L = GroupLayout<BN, STAGES, NACC>;
-  constexpr int HALF = BN / 2;
+  using L = GroupLayout<BN, STAGES, NACC, SPLIT, RS>;
+  constexpr int HALF = L::WCOLS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
@@ -480,7 +490,7 @@ __global__ void __launch_bounds__(kGroupThreads, 1)
     }
     for (int i = 0; i < NACC; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], kGroupEpiWarps);
+      mbar_init(&tempty[i], L::EPI_WARPS);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -495,6 +505,11 @@ __global__ void __launch_bounds__(kGroupThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
+  // With RS, registers move from warpgroup 0 (one TMA thread, one MMA thread) to
+  // the epilogue warpgroups; the host launches this form only when the shares add
+  // up to the block's registers.
+  if (warp < L::FIRST_EPI) {
+  if constexpr (RS) setmaxnreg_dec<L::REG_LO>();
   if (warp == 0) {
     // ------------------------------------------------------------- producer
     if (lane == 0) {
@@ -562,11 +577,13 @@ __global__ void __launch_bounds__(kGroupThreads, 1)
       volatile int never = 0;
       mbar_wait(drain, 0, &never, p.status, p.timeout_ns);
     }
+  }
   } else {
+    if constexpr (RS) setmaxnreg_inc<L::REG_HI>();
     // ------------------------------------------------------------- epilogue
-    const int ew = warp - 2;
+    const int ew = warp - L::FIRST_EPI;
     const int q = warp & 3;                   // TMEM lane quarter this warp may access
-    const int h = ew >> 2;                    // column half
+    const int h = ew >> 2;                    // column slice
     uint8_t* stage_buf = smem + L::OFF_D + ew * 2 * L::D_BYTES;
     int dbuf = 0;
     uint32_t acc_i = 0;
@@ -578,10 +595,10 @@ __global__ void __launch_bounds__(kGroupThreads, 1)
       const int row = mb * BM + q * 32 + lane;
       const int r0 = mb * BM + q * 32;
       const int nbase = nb * BN;
-      f32x2_t accum[HALF / 2];
+      float accum[HALF];
 #pragma unroll
-      for (int j = 0; j < HALF / 2; ++j) accum[j] = 0ull;
-      const ScaleStream<AMODE, BBLOCK> ss(p, row, nbase);
+      for (int j = 0; j < HALF; ++j) accum[j] = 0.0f;
+      const ScaleStream<AMODE, BBLOCK> ss(p, row, nbase + h * HALF);
       uint32_t ra[kScalePrefetch];
       float rb[kScalePrefetch];
 #pragma unroll
@@ -589,7 +606,6 @@ __global__ void __launch_bounds__(kGroupThreads, 1)
         ra[i] = ss.a_raw(i);
         rb[i] = ss.b_raw(i);
       }
-#pragma unroll 4
       for (int kb = 0; kb < p.num_kb; ++kb) {
         const uint32_t a_raw = ra[0];
         const float b_raw = rb[0];
@@ -604,36 +620,48 @@ __global__ void __launch_bounds__(kGroupThreads, 1)
         ok = mbar_wait(&tfull[acc], (acc_i / NACC) & 1u, abort_flag, p.status, p.timeout_ns);
         if (!ok) break;
         tc_fence_after();
-        uint32_t r0v[32], r1v[32];
-        tmem_ld_32x32b_x32(lane_addr + acc * BN, r0v);
-        tmem_ld_32x32b_x32(lane_addr + acc * BN + 32, r1v);
-        tmem_ld_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[acc]);
         const float sk = ScaleStream<AMODE, BBLOCK>::decode(a_raw, kb) * b_raw;
-        const f32x2_t sk2 = pack_f2(__float_as_uint(sk), __float_as_uint(sk));
+        // 32-column chunks; the buffer goes back to the MMA warp once its last chunk is
+        // in registers
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          accum[j] = fma_f2(sk2, pack_f2(r0v[2 * j], r0v[2 * j + 1]), accum[j]);
-          accum[16 + j] = fma_f2(sk2, pack_f2(r1v[2 * j], r1v[2 * j + 1]), accum[16 + j]);
+        for (int c = 0; c < HALF / 32; ++c) {
+          uint32_t rv[32];
+          tmem_ld_32x32b_x32(lane_addr + acc * BN + c * 32, rv);
+          tmem_ld_wait();
+          if (c + 1 == HALF / 32) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[acc]);
+          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j) accum[c * 32 + j] = fmaf(sk, __uint_as_float(rv[j]), accum[c * 32 + j]);
         }
         ++acc_i;
       }
       if (!ok) break;
+      // column scale (per tensor or per column; block scales were applied per K block)
+      // and bias, two columns at a time (N is a multiple of 8, so n < N covers n + 1)
+      const float sb_t = p.b_mode == 0 ? __ldg(p.b_scale) : 1.0f;
 #pragma unroll
       for (int c = 0; c < HALF / 32; ++c) {
         const int n0 = nbase + h * HALF + c * 32;
-        float sb[32], bs[32];
-        load_col_vectors(p, n0, sb, bs);
         uint32_t w[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          float a0, a1;
-          unpack_f2(accum[c * 16 + j], a0, a1);
-          const float v0 = a0 * sb[2 * j] + bs[2 * j];
-          const float v1 = a1 * sb[2 * j + 1] + bs[2 * j + 1];
-          w[j] = pack2(v0, v1, p.out_fp16);
+          const int n = n0 + 2 * j;
+          float s0 = sb_t, s1 = sb_t, b0 = 0.0f, b1 = 0.0f;
+          if (n < p.N) {
+            if (p.b_mode == 1) {
+              s0 = __ldg(p.b_scale + n);
+              s1 = __ldg(p.b_scale + n + 1);
+            }
+            if (p.bias) {
+              b0 = __bfloat162float(p.bias[n]);
+              b1 = __bfloat162float(p.bias[n + 1]);
+            }
+          }
+          const float a0 = accum[c * 32 + 2 * j], a1 = accum[c * 32 + 2 * j + 1];
+          w[j] = pack2(a0 * s0 + b0, a1 * s1 + b1, p.out_fp16);
         }
         if (store_block(&tmD, stage_buf + dbuf * L::D_BYTES, w, lane, n0, r0, p.M, p.N)) dbuf ^= 1;
       }
@@ -876,41 +904,73 @@ cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorM
   return cudaGetLastError();
 }
 
-constexpr int kGroupBN = 128, kGroupStages = 6, kGroupAcc = 4;
+// Group-scale tiles: 128 x 256 with two accumulators and a register split (the
+// preferred form), or 128 x 192 without one.  The split is used only if the kernel
+// was built with the register count its setmaxnreg shares assume.
+constexpr int kGroupBN = 256;
+constexpr int kGroupBNAlt = 192;
 
 template <int AMODE, bool BBLOCK>
-cudaError_t launch_group(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td, const GemmArgs& p,
-                         int grid, cudaStream_t st) {
-  using L = GroupLayout<kGroupBN, kGroupStages, kGroupAcc>;
-  auto kern = fp8_gemm_group_kernel<kGroupBN, kGroupStages, kGroupAcc, AMODE, BBLOCK>;
-  static int configured_dev = -1;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (configured_dev != dev) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
-    if (e != cudaSuccess) return e;
-    configured_dev = dev;
+struct GroupKernels {
+  using LS = GroupLayout<kGroupBN, 4, 2, 2, true>;
+  using LA = GroupLayout<kGroupBNAlt, 4, 2, 3, false>;
+  static constexpr auto split = fp8_gemm_group_kernel<kGroupBN, 4, 2, 2, true, AMODE, BBLOCK>;
+  static constexpr auto alt = fp8_gemm_group_kernel<kGroupBNAlt, 4, 2, 3, false, AMODE, BBLOCK>;
+
+  // Once per device: shared-memory opt-in for both, and whether the split kernel's
+  // register count covers its setmaxnreg shares (otherwise its warps would wait).
+  static cudaError_t prepare(bool* split_ok) {
+    static int dev_done = -1;
+    static bool ok = false;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev_done != dev) {
+      cudaError_t e = cudaFuncSetAttribute(split, cudaFuncAttributeMaxDynamicSharedMemorySize, LS::ALLOC);
+      if (e == cudaSuccess) e = cudaFuncSetAttribute(alt, cudaFuncAttributeMaxDynamicSharedMemorySize, LA::ALLOC);
+      cudaFuncAttributes fa;
+      if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, split);
+      if (e != cudaSuccess) return e;
+      ok = 128 * LS::REG_LO + 32 * LS::EPI_WARPS * LS::REG_HI <= LS::THREADS * fa.numRegs;
+      dev_done = dev;
+    }
+    *split_ok = ok;
+    return cudaSuccess;
   }
-  kern<<<grid, kGroupThreads, L::ALLOC, st>>>(ta, tb, td, p);
-  return cudaGetLastError();
+
+  static cudaError_t launch(bool use_split, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td,
+                            const GemmArgs& p, int grid, cudaStream_t st) {
+    if (use_split)
+      split<<<grid, LS::THREADS, LS::ALLOC, st>>>(ta, tb, td, p);
+    else
+      alt<<<grid, LA::THREADS, LA::ALLOC, st>>>(ta, tb, td, p);
+    return cudaGetLastError();
+  }
+};
+
+// The runtime scale modes mapped onto the compiled specialisations.
+#define FP8MM_GROUP_DISPATCH(a_mode, bblock, CALL)                                              \
+  do {                                                                                          \
+    if (bblock) {                                                                               \
+      if ((a_mode) == FP8MM_SCALE_A_GROUP128) return GroupKernels<FP8MM_SCALE_A_GROUP128, true>::CALL; \
+      if ((a_mode) == FP8MM_SCALE_A_GROUP128_COLMAJOR)                                          \
+        return GroupKernels<FP8MM_SCALE_A_GROUP128_COLMAJOR, true>::CALL;                       \
+      return GroupKernels<FP8MM_SCALE_A_GROUP128_UE8M0, true>::CALL;                            \
+    }                                                                                           \
+    if ((a_mode) == FP8MM_SCALE_A_GROUP128) return GroupKernels<FP8MM_SCALE_A_GROUP128, false>::CALL; \
+    if ((a_mode) == FP8MM_SCALE_A_GROUP128_COLMAJOR)                                            \
+      return GroupKernels<FP8MM_SCALE_A_GROUP128_COLMAJOR, false>::CALL;                        \
+    return GroupKernels<FP8MM_SCALE_A_GROUP128_UE8M0, false>::CALL;                             \
+  } while (0)
+
+cudaError_t group_prepare(int a_mode, bool bblock, bool* split_ok) {
+  FP8MM_GROUP_DISPATCH(a_mode, bblock, prepare(split_ok));
 }
 
-template <bool BBLOCK>
-cudaError_t launch_group_a(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td, const GemmArgs& p,
-                           int grid, cudaStream_t st) {
-  switch (p.a_mode) {
-    case FP8MM_SCALE_A_GROUP128: return launch_group<FP8MM_SCALE_A_GROUP128, BBLOCK>(ta, tb, td, p, grid, st);
-    case FP8MM_SCALE_A_GROUP128_COLMAJOR:
-      return launch_group<FP8MM_SCALE_A_GROUP128_COLMAJOR, BBLOCK>(ta, tb, td, p, grid, st);
-    default: return launch_group<FP8MM_SCALE_A_GROUP128_UE8M0, BBLOCK>(ta, tb, td, p, grid, st);
-  }
+cudaError_t group_launch(int a_mode, bool bblock, bool use_split, const CUtensorMap& ta, const CUtensorMap& tb,
+                         const CUtensorMap& td, const GemmArgs& p, int grid, cudaStream_t st) {
+  FP8MM_GROUP_DISPATCH(a_mode, bblock, launch(use_split, ta, tb, td, p, grid, st));
 }
-
-cudaError_t launch_group_modes(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td,
-                               const GemmArgs& p, int grid, cudaStream_t st) {
-  return p.b_mode == 2 ? launch_group_a<true>(ta, tb, td, p, grid, st)
-                       : launch_group_a<false>(ta, tb, td, p, grid, st);
-}
+#undef FP8MM_GROUP_DISPATCH
 
 int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
 
@@ -957,7 +1017,7 @@ int pick_splits(int64_t M, int64_t N, int num_kb, int sms) {
 // Shape-keyed tile table.  Deterministic mode picks its tile from N alone, so every M
 // (and every prefix / suffix of the rows) runs the same tile, K order and instruction.
 Config pick_config(int64_t M, int64_t N, bool deterministic, bool group_a, int sms) {
-  if (group_a) return {kGroupBN, kGroupStages, true};
+  if (group_a) return {kGroupBN, 4, true};
   if (deterministic) {
     if (N >= 1024) return {256, 4, false};
     if (N >= 256) return {128, 6, false};
@@ -1049,7 +1109,13 @@ extern "C" int fp8_scaled_mm(const void* A, const void* B, const float* a_scale,
     return e == cudaSuccess ? FP8MM_OK : FP8MM_ECUDA;
   }
 
-  const Config cfg = pick_config(M, N, deterministic != 0, group_a, sms);
+  Config cfg = pick_config(M, N, deterministic != 0, group_a, sms);
+  bool group_split = false;
+  if (group_a) {
+    const cudaError_t e = group_prepare(a_mode, b_mode == 2, &group_split);
+    if (e != cudaSuccess) return FP8MM_ECUDA;
+    if (!group_split) cfg.bn = kGroupBNAlt;
+  }
   CUtensorMap ta, tb, td;
   if (!make_tma_2d(&ta, const_cast<void*>(A), CU_TENSOR_MAP_DATA_TYPE_UINT8, K, M, lda, BK, BM,
                    CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -1075,7 +1141,7 @@ extern "C" int fp8_scaled_mm(const void* A, const void* B, const float* a_scale,
   const int grid = p.tiles < sms ? p.tiles : sms;
   cudaError_t e;
   if (cfg.group_a)
-    e = launch_group_modes(ta, tb, td, p, grid, st);
+    e = group_launch(a_mode, b_mode == 2, group_split, ta, tb, td, p, grid, st);
   else if (cfg.bn == 256)
     e = launch<256, 4>(ta, tb, td, p, grid, st);
   else if (cfg.bn == 128)
