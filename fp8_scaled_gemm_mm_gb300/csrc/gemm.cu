@@ -702,7 +702,8 @@ struct SwapLayout {
   static constexpr int OFF_BAR = DATA;
   static constexpr int NBARS = 2 * STAGES + 2;
   static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
-  static constexpr int ALLOC = OFF_MISC + 16 + 1024;
+  static constexpr int OFF_VEC = (OFF_MISC + 16 + 15) / 16 * 16;   // b_scale[128], bias[128], a_scale[BT]
+  static constexpr int ALLOC = OFF_VEC + (256 + BT) * 4 + 1024;
   static constexpr uint32_t TMEM_COLS = pow2_at_least(BT);
   static_assert(X_BYTES % 1024 == 0, "token block must keep 1024-byte alignment");
 };
@@ -725,6 +726,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* drain = tfull + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
+  float* vec_sb = reinterpret_cast<float*>(smem + L::OFF_VEC);
+  float* vec_bias = vec_sb + 128;
+  float* vec_sa = vec_bias + 128;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -736,6 +740,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kb0 = static_cast<int>(static_cast<int64_t>(rank) * p.num_kb / S);
   const int kb1 = static_cast<int>(static_cast<int64_t>(rank + 1) * p.num_kb / S);
 
+  // The first ring's worth of loads is issued by the producer thread right after the
+  // barriers exist, before TMEM allocation and the block barrier.
+  const int pre = kb1 - kb0 < L::STAGES ? kb1 - kb0 : L::STAGES;
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmX);
@@ -747,7 +754,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
+    for (int j = 0; j < pre; ++j) {
+      mbar_arrive_expect_tx(&full[j], L::W_BYTES + L::X_BYTES);
+      uint8_t* st = smem + j * (L::W_BYTES + L::X_BYTES);
+      tma_load_2d(&tmW, &full[j], st, (kb0 + j) * BK, n0);
+      tma_load_2d(&tmX, &full[j], st + L::W_BYTES, (kb0 + j) * BK, m0);
+    }
   }
+
   if (warp == 1) {
     tmem_alloc(tmem_slot, L::TMEM_COLS);
     tmem_relinquish();
@@ -760,9 +774,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      uint32_t stage = 0, phase = 0;
-      int issued = 0;
-      for (int kb = kb0; kb < kb1; ++kb) {
+      uint32_t stage = pre % L::STAGES, phase = pre == L::STAGES ? 1u : 0u;
+      int issued = pre;
+      for (int kb = kb0 + pre; kb < kb1; ++kb) {
         if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status, p.timeout_ns)) break;
         mbar_arrive_expect_tx(&full[stage], L::W_BYTES + L::X_BYTES);
         uint8_t* st = smem + stage * (L::W_BYTES + L::X_BYTES);
@@ -812,6 +826,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(drain, 0, &never, p.status, p.timeout_ns);
     }
   } else {
+    {
+      // the epilogue's column scales, bias and row scales, fetched while the weights stream
+      const int t = threadIdx.x - 64;
+      const int n = n0 + t;
+      vec_sb[t] = n < p.N ? (p.b_mode == 0 ? __ldg(p.b_scale) : __ldg(p.b_scale + n)) : 0.0f;
+      vec_bias[t] = (p.bias && n < p.N) ? __bfloat162float(p.bias[n]) : 0.0f;
+      for (int m = t; m < BT; m += 128) vec_sa[m] = a_scale_at(p, m0 + m, 0);
+    }
     // TMEM -> own shared-memory partial [BT][128] (lane = weight row within the tile)
     const int q = warp & 3;
     const int row = q * 32 + lane;
@@ -843,31 +865,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int total = quads * mt;
     const uint32_t part_addr = smem_u32(part);
     const bool no_abort = *abort_flag == 0;
-    for (int idx = t; idx < total && no_abort; idx += 128) {
-      const int m = idx / quads;
-      const int row = r_begin + 4 * (idx - m * quads);
-      const int n = n0 + row;
-      if (n >= p.N) continue;
-      const uint32_t off = static_cast<uint32_t>((m * 128 + row) * 4);
-      float4 acc = ld_dsmem_f32x4(mapa_shared(part_addr + off, 0));
-      for (int s2 = 1; s2 < S; ++s2) {
-        const float4 v = ld_dsmem_f32x4(mapa_shared(part_addr + off, static_cast<uint32_t>(s2)));
-        acc.x += v.x;
-        acc.y += v.y;
-        acc.z += v.z;
-        acc.w += v.w;
-      }
-      const float sa = a_scale_at(p, m0 + m, 0);
-      float sb[4], bs[4];
+    // four outputs (x 4 rows) per thread per pass, their S partial loads in flight together
+    constexpr int U = 4;
+    for (int base = t; base < total && no_abort; base += 128 * U) {
+      float4 acc[U];
+      uint32_t offs[U];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        sb[j] = p.b_mode == 0 ? __ldg(p.b_scale) : __ldg(p.b_scale + n + j);
-        bs[j] = p.bias ? __bfloat162float(p.bias[n + j]) : 0.0f;
+      for (int u = 0; u < U; ++u) {
+        const int idx = base + u * 128;
+        const int m = idx < total ? idx / quads : 0;
+        const int row = idx < total ? r_begin + 4 * (idx - m * quads) : r_begin;
+        offs[u] = static_cast<uint32_t>((m * 128 + row) * 4);
+        acc[u] = ld_dsmem_f32x4(mapa_shared(part_addr + offs[u], 0));
       }
-      const float v0 = acc.x * sa * sb[0] + bs[0], v1 = acc.y * sa * sb[1] + bs[1];
-      const float v2 = acc.z * sa * sb[2] + bs[2], v3 = acc.w * sa * sb[3] + bs[3];
-      const int64_t o = static_cast<int64_t>(m0 + m) * p.N + n;
-      *reinterpret_cast<uint2*>(out + o) = make_uint2(pack2(v0, v1, p.out_fp16), pack2(v2, v3, p.out_fp16));
+#pragma unroll 1
+      for (int s2 = 1; s2 < S; ++s2) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const float4 v = ld_dsmem_f32x4(mapa_shared(part_addr + offs[u], static_cast<uint32_t>(s2)));
+          acc[u].x += v.x;
+          acc[u].y += v.y;
+          acc[u].z += v.z;
+          acc[u].w += v.w;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int idx = base + u * 128;
+        if (idx >= total) break;
+        const int m = idx / quads;
+        const int row = r_begin + 4 * (idx - m * quads);
+        const int n = n0 + row;
+        if (n >= p.N) continue;
+        const float sa = vec_sa[m];
+        const float4 sb = *reinterpret_cast<const float4*>(vec_sb + row);
+        const float4 bs = *reinterpret_cast<const float4*>(vec_bias + row);
+        const float v0 = acc[u].x * sa * sb.x + bs.x, v1 = acc[u].y * sa * sb.y + bs.y;
+        const float v2 = acc[u].z * sa * sb.z + bs.z, v3 = acc[u].w * sa * sb.w + bs.w;
+        const int64_t o = static_cast<int64_t>(m0 + m) * p.N + n;
+        *reinterpret_cast<uint2*>(out + o) = make_uint2(pack2(v0, v1, p.out_fp16), pack2(v2, v3, p.out_fp16));
+      }
     }
   }
 
