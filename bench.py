@@ -236,9 +236,10 @@ def run_gpu(args, rank, world, local_rank):
     if rank == 0:
         quant_obj = bench_group_quant(torch, fm, synth, dev, flush)
 
-    widened = None
+    widened = per_tensor = None
     if rank == 0:
         widened = bench_widened(torch, fm, synth, dev, flush, work[0])
+        per_tensor = bench_per_tensor(torch, fm, dev, flush)
 
     # ---- end to end through the C ABI with host buffers
     e2e = None
@@ -247,7 +248,7 @@ def run_gpu(args, rank, world, local_rank):
 
     res = dict(step_ms=tot_step_ms / args.steps, gemm_ms=tot_gemm_ms / args.steps,
                quant_ms=tot_quant_ms / args.steps, wall=wall, step_flops=step_flops,
-               step_quant_bytes=step_quant_bytes, clocks=clocks, quant=quant_obj, e2e=e2e, widened=widened,
+               step_quant_bytes=step_quant_bytes, clocks=clocks, quant=quant_obj, e2e=e2e, widened=widened, per_tensor=per_tensor,
                per_shape_gemm_ms=[x / args.steps for x in per_shape_gemm], launches=2 * len(work) * args.steps)
     return res
 
@@ -363,6 +364,32 @@ def bench_widened(torch, fm, synth, dev, flush, w0, reps=10):
     for v in out.values():
         if "bytes" in v:
             v["gbs"] = round(v["bytes"] / (v["us"] * 1e-6) / 1e9, 1)
+    return out
+
+
+def bench_per_tensor(torch, fm, dev, flush, reps=10):
+    """Per-tensor scaled GEMMs at K = 4096 for every (M, N) of the per-tensor
+    configuration (M in 1, 16, 128, 2048, 8192; N in 4096, 12288, 14336), L2 flushed
+    before each timed launch.  M <= 128 is HBM-bound (the weight streams once),
+    larger M tensor-bound."""
+    K = 4096
+    g = torch.Generator(device=dev).manual_seed(11)
+    out = []
+    for N in (4096, 12288, 14336):
+        B = torch.randint(0, 126, (N, K), generator=g, dtype=torch.uint8, device=dev)
+        for M in (1, 16, 128, 2048, 8192):
+            A = torch.randint(0, 126, (M, K), generator=g, dtype=torch.uint8, device=dev)
+            a_s = torch.full((1,), 0.02, dtype=torch.float32, device=dev)
+            b_s = torch.full((1,), 0.001, dtype=torch.float32, device=dev)
+            D = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            us = _median_us(torch, flush, lambda: fm.fp8_scaled_mm(A, B, a_s, b_s, fm.A_TENSOR | fm.B_TENSOR, D),
+                            reps)
+            nbytes = M * K + N * K + 2 * M * N
+            out.append({"M": M, "N": N, "K": K, "us": round(us, 2),
+                        "tflops": round(flops(M, K, N) / (us * 1e-6) / 1e12, 1),
+                        "gbs": round(nbytes / (us * 1e-6) / 1e9, 1), "bound": "hbm" if M <= 128 else "tensor"})
+            del A, D
+        del B
     return out
 
 
@@ -636,6 +663,11 @@ def main():
             if "tflops" in v:
                 v["frac_fp8_peak"] = round(v["tflops"] / fp8_peak, 4)
         line["widened"] = wd
+    if res["per_tensor"]:
+        for v in res["per_tensor"]:
+            v["frac"] = round(v["gbs"] / hbm_peak if v["bound"] == "hbm" else v["tflops"] / fp8_peak, 4)
+        line["per_tensor_k4096"] = {"note": "per-tensor scales, L2 flushed before each launch, event-timed; "
+                                            "frac of HBM (M <= 128) or of the FP8 peak", "shapes": res["per_tensor"]}
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_rows)
     print(json.dumps(line), flush=True)

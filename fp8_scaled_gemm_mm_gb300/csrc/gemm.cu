@@ -865,34 +865,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int total = quads * mt;
     const uint32_t part_addr = smem_u32(part);
     const bool no_abort = *abort_flag == 0;
-    // four outputs (x 4 rows) per thread per pass, their S partial loads in flight together
-    constexpr int U = 4;
+    // two outputs (x 4 rows) per thread per pass; all S partial loads of both are issued
+    // before any is summed (S <= 8), then summed in rank order
+    constexpr int U = 2;
     for (int base = t; base < total && no_abort; base += 128 * U) {
-      float4 acc[U];
-      uint32_t offs[U];
+      float4 pv[U][8];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int idx = base + u * 128;
         const int m = idx < total ? idx / quads : 0;
         const int row = idx < total ? r_begin + 4 * (idx - m * quads) : r_begin;
-        offs[u] = static_cast<uint32_t>((m * 128 + row) * 4);
-        acc[u] = ld_dsmem_f32x4(mapa_shared(part_addr + offs[u], 0));
-      }
-#pragma unroll 1
-      for (int s2 = 1; s2 < S; ++s2) {
+        const uint32_t off = static_cast<uint32_t>((m * 128 + row) * 4);
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const float4 v = ld_dsmem_f32x4(mapa_shared(part_addr + offs[u], static_cast<uint32_t>(s2)));
-          acc[u].x += v.x;
-          acc[u].y += v.y;
-          acc[u].z += v.z;
-          acc[u].w += v.w;
-        }
+        for (int s2 = 0; s2 < 8; ++s2)
+          if (s2 < S) pv[u][s2] = ld_dsmem_f32x4(mapa_shared(part_addr + off, static_cast<uint32_t>(s2)));
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int idx = base + u * 128;
         if (idx >= total) break;
+        float4 acc = pv[u][0];
+#pragma unroll
+        for (int s2 = 1; s2 < 8; ++s2) {
+          if (s2 < S) {
+            acc.x += pv[u][s2].x;
+            acc.y += pv[u][s2].y;
+            acc.z += pv[u][s2].z;
+            acc.w += pv[u][s2].w;
+          }
+        }
         const int m = idx / quads;
         const int row = r_begin + 4 * (idx - m * quads);
         const int n = n0 + row;
@@ -900,8 +901,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float sa = vec_sa[m];
         const float4 sb = *reinterpret_cast<const float4*>(vec_sb + row);
         const float4 bs = *reinterpret_cast<const float4*>(vec_bias + row);
-        const float v0 = acc[u].x * sa * sb.x + bs.x, v1 = acc[u].y * sa * sb.y + bs.y;
-        const float v2 = acc[u].z * sa * sb.z + bs.z, v3 = acc[u].w * sa * sb.w + bs.w;
+        const float v0 = acc.x * sa * sb.x + bs.x, v1 = acc.y * sa * sb.y + bs.y;
+        const float v2 = acc.z * sa * sb.z + bs.z, v3 = acc.w * sa * sb.w + bs.w;
         const int64_t o = static_cast<int64_t>(m0 + m) * p.N + n;
         *reinterpret_cast<uint2*>(out + o) = make_uint2(pack2(v0, v1, p.out_fp16), pack2(v2, v3, p.out_fp16));
       }
@@ -1043,11 +1044,17 @@ cudaError_t launch_swap(const CUtensorMap& tw, const CUtensorMap& tx, const Gemm
 }
 
 // Split count for the small-M path: as many K slices (cluster size <= 8, at least two
-// K blocks each) as keep every CTA resident at two CTAs per SM.
+// K blocks each) as keep every CTA resident at two CTAs per SM, and no more than keep
+// the fp32 partials (S x token block x 128 x 4 bytes, written then read) under half
+// the weight bytes of a tile.
 int pick_splits(int64_t M, int64_t N, int num_kb, int sms) {
   const int64_t tiles = static_cast<int64_t>(ceil_div(N, 128)) * ceil_div(M, 128);
   int s = 1;
-  while (s < 8 && tiles * (s + 1) <= 2LL * sms && (s + 1) * 2 <= num_kb) ++s;
+  // the partials written and read back grow with S x token block; keep them below
+  // half the weight slice a cluster streams
+  const int64_t bt = M <= 16 ? 16 : (M <= 32 ? 32 : (M <= 64 ? 64 : 128));
+  const int64_t cap = static_cast<int64_t>(num_kb) * BK / (16 * bt);
+  while (s < 8 && s + 1 <= cap && tiles * (s + 1) <= 2LL * sms && (s + 1) * 2 <= num_kb) ++s;
   return s;
 }
 
