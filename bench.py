@@ -135,6 +135,21 @@ class ClockSampler:
 
 # ------------------------------------------------------------ multi-rank
 
+class L2Flush:
+    """Evicts the L2 between timed launches: writes a buffer four times the L2, then
+    reads another as large, so that the L2 holds neither the timed kernel's data nor
+    dirty lines whose write-back the next kernel would pay for."""
+
+    def __init__(self, torch, dev):
+        self.w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+        self.r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self.sink = torch.empty((), dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        self.w.zero_()
+        self.sink.copy_(self.r.sum())   # a plain fp32 reduction: reads the buffer, writes a scalar
+
+
 def max_over_ranks(values, device="cpu"):
     """Element-wise maximum of per-rank timings over the process group (every
     rank receives the result); the job is as slow as its slowest rank."""
@@ -175,7 +190,7 @@ def run_gpu(args, rank, world, local_rank):
         a_s = torch.empty((M, 1), dtype=torch.float32, device=dev)
         D = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
         work.append(dict(M=M, K=K, N=N, X=X, A=A, a_s=a_s, B=B, b_s=b_s, D=D))
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    flush = L2Flush(torch, dev)
     torch.cuda.synchronize()
 
     step_flops = sum(flops(w["M"], w["K"], w["N"]) for w in work)
@@ -192,7 +207,7 @@ def run_gpu(args, rank, world, local_rank):
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_events)] for _ in range(args.steps)]
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         step([torch.cuda.Event(enable_timing=True) for _ in range(n_events)])
     torch.cuda.synchronize()
 
@@ -205,7 +220,7 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for k in range(args.steps):
-        flush.zero_()                       # L2 flush between timed steps (not inside them)
+        flush()                       # L2 flush between timed steps (not inside them)
         step(evs[k])
     torch.cuda.synchronize()
     if world > 1:
@@ -263,7 +278,7 @@ def bench_group_quant(torch, fm, synth, dev, flush, reps=20):
             fm.per_token_group_quant_fp8(x, q, s, 128, fm.SCALE_UE8M0_PACKED, True, fuse)
         ts = []
         for _ in range(reps):
-            flush.zero_()
+            flush()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
             fm.per_token_group_quant_fp8(x, q, s, 128, fm.SCALE_UE8M0_PACKED, True, fuse)
@@ -287,7 +302,7 @@ def bench_group_quant(torch, fm, synth, dev, flush, reps=20):
         fm.silu_and_mul_masked_post_quant_fp8(xm, mm, qm, sm, 128)
     ts = []
     for _ in range(reps):
-        flush.zero_()
+        flush()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
         fm.silu_and_mul_masked_post_quant_fp8(xm, mm, qm, sm, 128)
@@ -307,7 +322,7 @@ def _median_us(torch, flush, fn, reps):
         fn()
     ts = []
     for _ in range(reps):
-        flush.zero_()
+        flush()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
         fn()
@@ -415,7 +430,7 @@ def bench_e2e(torch, fm, work, flush, args):
     torch.cuda.synchronize()
     times = []
     for _ in range(steps):
-        flush.zero_()
+        flush()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         one()
@@ -625,7 +640,8 @@ def main():
         "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights, bf16, quantized on device)",
         "config": {"workload": "large rowwise-scaled FP8 prefill GEMMs (5 shapes) + per-token activation quant",
                    "shapes_MxKxN": [list(s) for s in SHAPES], "out": "bf16", "scales": "fp32 per-row x per-col",
-                   "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write), outside the step events",
+                   "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write, then {L2_FLUSH_BYTES >> 20} "
+                         "MiB read so no dirty lines remain), outside the step events",
                    "parallelism": f"replicas x{world} (no data-path collective)"},
         "gemm": {"tflops": round(gemm_tflops, 2), "ms_per_step": round(res["gemm_ms"], 4),
                  "per_shape_tflops": [round(flops(*s) / (t * 1e-3) / 1e12, 1)

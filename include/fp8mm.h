@@ -176,6 +176,7 @@ FP8MM_API int per_token_group_quant_fp8_scatter(const void* x, int x_dtype, cons
  *            int32 [E, ceil(G/4), pad4(T)].
  *   masked_m int32 [E], device; values outside [0, T] are clamped and
  *            recorded as FP8MM_EINVAL in the device status word.
+ *   E        at most 1024 (each CTA stages masked_m in shared memory).
  *   group    32, 64 or 128.  Requirements as per_token_group_quant_fp8.
  */
 FP8MM_API int silu_and_mul_masked_post_quant_fp8(const void* x, int x_dtype, const int32_t* masked_m, int64_t E,

@@ -94,3 +94,26 @@ def test_gemm_argument_validation(L):
     assert call(out=f + 16) == -1                     # out overlaps A
     assert call(M=0) == 0                             # empty: no launch
     assert call(A=None) == -1
+
+
+def test_masked_and_new_entry_validation(L):
+    f = 1 << 20
+    m = L.silu_and_mul_masked_post_quant_fp8
+    # more experts than a CTA stages, T not positive, bad group: rejected before any launch
+    assert m(f, 0, f, 1025, 64, 256, f, f, 128, 2, 1, None) == -1
+    assert m(f, 0, f, 4, -1, 256, f, f, 128, 2, 1, None) == -1
+    assert m(f, 0, f, 4, 64, 256, f, f, 96, 2, 1, None) == -1
+    assert m(None, 0, None, 0, 64, 256, None, None, 128, 2, 1, None) == 0     # no experts: no-op
+    i8 = L.per_token_group_quant_int8
+    assert i8(f, 0, f, f, 4, 2048, 96, 0, 0, None) == -1                   # bad group
+    assert i8(f, 0, f + 8, f, 4, 2048, 128, 0, 0, None) == -2              # misaligned codes
+    rp = L.per_token_group_quant_fp8_row_padded
+    assert rp(f, 0, f, f, 8, 4, 128, 128, 0, 1, None) == -1                # M_pad < M
+    assert rp(f, 0, f, f, 8, 16, 128, 128, 3, 1, None) == -1               # bad format
+    sq = L.static_per_tensor_quant_fp8
+    assert sq(f, 0, f, f, 24, None) == -1                                   # numel % 16
+    assert sq(f, 2, f, f, 32, None) == -1                                   # bad dtype
+    rq = L.requantize_with_max_scale_fp8
+    w = (ctypes.c_int64 * 2)(6, 6)
+    assert rq(f, f, f, ctypes.cast(w, ctypes.c_void_p), 2, 8, 32, f, None) == -1   # shards past N
+    assert rq(f, f, f, ctypes.cast(w, ctypes.c_void_p), 0, 8, 32, f, None) == -1   # no shards
