@@ -409,14 +409,12 @@ struct GroupLayout {
   static_assert(ALLOC <= 232448, "shared memory budget");
 };
 
-// The scales of K block kb are fetched kScalePrefetch blocks ahead as raw words and
-// decoded when used, so no arithmetic waits on the load.
-constexpr int kScalePrefetch = 4;
-
 // Scale stream of one epilogue thread for the K blocks of a tile: A scale words of
 // its row (AMODE fixes the layout at compile time) and, with BBLOCK, the block B
 // scale of the tile's 128 columns.  Rows past M read row M-1 and K blocks past the
-// end read the last one; neither value is used.
+// end read the last one; neither value is used.  The epilogue fetches the words of a
+// group of four K blocks one group ahead and decodes them when used, so no
+// arithmetic waits on a load.
 template <int AMODE, bool BBLOCK>
 struct ScaleStream {
   const uint32_t* a;
@@ -599,44 +597,55 @@ __global__ void __launch_bounds__(GroupLayout<BN, STAGES, NACC, SPLIT, RS>::THRE
 #pragma unroll
       for (int j = 0; j < HALF; ++j) accum[j] = 0.0f;
       const ScaleStream<AMODE, BBLOCK> ss(p, row, nbase + h * HALF);
-      uint32_t ra[kScalePrefetch];
-      float rb[kScalePrefetch];
+      // K blocks in groups of four: the scale words of the next group are loaded while
+      // this one is folded (a packed UE8M0 word holds all four A scales of a group)
+      constexpr bool PACKED = AMODE == FP8MM_SCALE_A_GROUP128_UE8M0;
+      uint32_t na[4];
+      float nbw[4];
 #pragma unroll
-      for (int i = 0; i < kScalePrefetch; ++i) {
-        ra[i] = ss.a_raw(i);
-        rb[i] = ss.b_raw(i);
+      for (int u = 0; u < 4; ++u) {
+        na[u] = (PACKED && u > 0) ? 0u : ss.a_raw(u);
+        nbw[u] = ss.b_raw(u);
       }
-      for (int kb = 0; kb < p.num_kb; ++kb) {
-        const uint32_t a_raw = ra[0];
-        const float b_raw = rb[0];
+      for (int kg = 0; kg < p.num_kb && ok; kg += 4) {
+        uint32_t ca[4];
+        float cb[4];
 #pragma unroll
-        for (int i = 0; i + 1 < kScalePrefetch; ++i) {
-          ra[i] = ra[i + 1];
-          rb[i] = rb[i + 1];
+        for (int u = 0; u < 4; ++u) {
+          ca[u] = na[u];
+          cb[u] = nbw[u];
         }
-        ra[kScalePrefetch - 1] = ss.a_raw(kb + kScalePrefetch);
-        rb[kScalePrefetch - 1] = ss.b_raw(kb + kScalePrefetch);
-        const uint32_t acc = acc_i % NACC;
-        ok = mbar_wait(&tfull[acc], (acc_i / NACC) & 1u, abort_flag, p.status, p.timeout_ns);
-        if (!ok) break;
-        tc_fence_after();
-        const float sk = ScaleStream<AMODE, BBLOCK>::decode(a_raw, kb) * b_raw;
-        // 32-column chunks; the buffer goes back to the MMA warp once its last chunk is
-        // in registers
 #pragma unroll
-        for (int c = 0; c < HALF / 32; ++c) {
-          uint32_t rv[32];
-          tmem_ld_32x32b_x32(lane_addr + acc * BN + c * 32, rv);
-          tmem_ld_wait();
-          if (c + 1 == HALF / 32) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty[acc]);
+        for (int u = 0; u < 4; ++u) {
+          na[u] = (PACKED && u > 0) ? 0u : ss.a_raw(kg + 4 + u);
+          nbw[u] = ss.b_raw(kg + 4 + u);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int kb = kg + u;
+          if (kb >= p.num_kb) break;
+          const uint32_t acc = acc_i % NACC;
+          ok = mbar_wait(&tfull[acc], (acc_i / NACC) & 1u, abort_flag, p.status, p.timeout_ns);
+          if (!ok) break;
+          tc_fence_after();
+          const float sk = ScaleStream<AMODE, BBLOCK>::decode(ca[PACKED ? 0 : u], kb) * cb[u];
+          // 32-column chunks; the buffer goes back to the MMA warp once its last chunk
+          // is in registers
+#pragma unroll
+          for (int c = 0; c < HALF / 32; ++c) {
+            uint32_t rv[32];
+            tmem_ld_32x32b_x32(lane_addr + acc * BN + c * 32, rv);
+            tmem_ld_wait();
+            if (c + 1 == HALF / 32) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&tempty[acc]);
+            }
+#pragma unroll
+            for (int j = 0; j < 32; ++j) accum[c * 32 + j] = fmaf(sk, __uint_as_float(rv[j]), accum[c * 32 + j]);
           }
-#pragma unroll
-          for (int j = 0; j < 32; ++j) accum[c * 32 + j] = fmaf(sk, __uint_as_float(rv[j]), accum[c * 32 + j]);
+          ++acc_i;
         }
-        ++acc_i;
       }
       if (!ok) break;
       // column scale (per tensor or per column; block scales were applied per K block)
