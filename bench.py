@@ -410,7 +410,10 @@ def bench_per_tensor(torch, fm, dev, flush, reps=10):
 
 def bench_e2e(torch, fm, work, flush, args):
     """Same step through the C ABI from pinned host buffers: H2D of each
-    activation, quant + GEMM, D2H of each output, all inside the timed region."""
+    activation, quant + GEMM, D2H of each output, all inside the timed region.
+    Copies in, compute and copies out run on three streams ordered by events, so
+    the copy of shape i+1's activation and of shape i-1's output overlap the
+    GEMM of shape i (every shape has its own buffers)."""
     host_x = [torch.empty(w["X"].shape, dtype=torch.bfloat16, pin_memory=True) for w in work]
     for hx, w in zip(host_x, work):
         hx.copy_(w["X"].cpu())
@@ -418,13 +421,25 @@ def bench_e2e(torch, fm, work, flush, args):
     h2d = sum(h.numel() * 2 for h in host_x)
     d2h = sum(h.numel() * 2 for h in host_d)
     steps = max(3, min(args.steps, 10))
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    s_cmp = torch.cuda.current_stream()
 
     def one():
-        for hx, hd, w in zip(host_x, host_d, work):
-            w["X"].copy_(hx, non_blocking=True)
-            fm.per_token_group_quant_fp8(w["X"], w["A"], w["a_s"], w["K"])
-            fm.fp8_scaled_mm(w["A"], w["B"], w["a_s"], w["b_s"], fm.A_ROW | fm.B_COL, w["D"])
-            hd.copy_(w["D"], non_blocking=True)
+        ev_in = [torch.cuda.Event() for _ in work]
+        ev_cmp = [torch.cuda.Event() for _ in work]
+        with torch.cuda.stream(s_in):
+            for i, (hx, w) in enumerate(zip(host_x, work)):
+                w["X"].copy_(hx, non_blocking=True)
+                ev_in[i].record(s_in)
+        for i, w in enumerate(work):
+            s_cmp.wait_event(ev_in[i])
+            fm.per_token_group_quant_fp8(w["X"], w["A"], w["a_s"], w["K"], stream=s_cmp)
+            fm.fp8_scaled_mm(w["A"], w["B"], w["a_s"], w["b_s"], fm.A_ROW | fm.B_COL, w["D"], stream=s_cmp)
+            ev_cmp[i].record(s_cmp)
+        with torch.cuda.stream(s_out):
+            for i, (hd, w) in enumerate(zip(host_d, work)):
+                s_out.wait_event(ev_cmp[i])
+                hd.copy_(w["D"], non_blocking=True)
 
     one()
     torch.cuda.synchronize()
