@@ -1,8 +1,8 @@
 #!/usr/bin/env python3
 """Benchmark of the FP8 linear hot path on GB300.
 
-One step = the five large rowwise-scaled prefill GEMMs of the pages' kernel
-table (sglang PR #34318, "Kernel results": M x K x N = 8320x5376x21504,
+One step = the five large rowwise-scaled prefill GEMMs of the kernel table of
+sglang PR #34318 ("Kernel results": M x K x N = 8320x5376x21504,
 8320x5376x14336, 23216x5376x28672, 15760x5376x28672, 8320x14336x5376), each
 preceded by the per-token quantization of its bf16 activation (group = K, fp32
 row scales) that produces the GEMM's A operand:
@@ -39,7 +39,7 @@ sys.path.insert(0, ROOT)
 METRIC = "FP8 scaled-GEMM TFLOP/s & % of FP8 peak; group-quant GB/s & % of HBM peak"
 SHAPES = [(8320, 5376, 21504), (8320, 5376, 14336), (23216, 5376, 28672), (15760, 5376, 28672),
           (8320, 14336, 5376)]  # (M, K, N)
-# torch._scaled_mm on H100 80GB for the same five shapes (pages' kernel table): sum 2MNK / sum time
+# torch._scaled_mm on H100 80GB for the same five shapes (sglang PR #34318, Kernel results): sum 2MNK / sum time
 H100_TORCH_US = [1351.1, 896.4, 5295.9, 3570.9, 843.9]
 QUANT_M, QUANT_K = 8192, 7168
 FP8_OVER_BF16 = 2.0      # nominal dense FP8 : BF16 tensor rate on GB300 (4.5 : 2.25 PFLOP/s)
@@ -650,7 +650,7 @@ def main():
         "scaling": "weak",
         "vs_baseline": round(value / world / h100_reference_tflops(), 3),
         "vs_baseline_note": "per-GPU value / torch._scaled_mm on H100 80GB for the same five shapes "
-                            f"({h100_reference_tflops():.0f} TFLOP/s, pages' kernel table; other hardware)",
+                            f"({h100_reference_tflops():.0f} TFLOP/s, sglang PR #34318 kernel table; other hardware)",
         "dtype": "e4m3 x e4m3 -> fp32 accumulate -> bf16",
         "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights, bf16, quantized on device)",
         "config": {"workload": "large rowwise-scaled FP8 prefill GEMMs (5 shapes) + per-token activation quant",

@@ -4,7 +4,7 @@ This module only draws random numbers and builds index structures; it holds
 none of the quantization or GEMM arithmetic, so both the CUDA path and the
 CPU oracle can be fed from it.
 
-Distributions follow the workloads of the pages:
+Distributions follow the workloads of the cited pull requests:
 * GEMM activations ~N(0, 1) and weights ~N(0, 0.02) in bf16, bias ~N(0, 0.1)
   (sglang PR #34318 "Route large SM90 row/column-scaled FP8 GEMMs to Torch",
   Kernel results table; sglang PR #44861 Modifications: bias, strided input,

@@ -7,7 +7,7 @@ with it.
 
 The arithmetic lives in ``fp8_oracle.c`` (plain C, IEEE fp32/fp64, no FMA
 contraction); this module marshals numpy arrays and lays scales out in the
-layouts the pages name, with plain indexing:
+layouts the cited pull requests name, with plain indexing:
 
 * per-token group quant -- sglang PR #33533 "[JIT] per_token_group_quant: fix
   the fp16 UE8M0 multiplier overflow, 1.23x on the fused EP-MoE path, unify

@@ -53,10 +53,11 @@
  *    sum stays below 2^33 * 2^18 = 2^51 < 2^53 ulps.  The result is scaled in
  *    fp64 and rounded once to bf16 / fp16 (round to nearest even).
  *
- *  - block scales (SURVEY's next step after the rowwise path; the pages name
- *    the block / MXFP8 GEMM, sglang PR #42865, without detail): A carries one
- *    scale per row and 128-wide K block, B one per 128 x 128 block, and
- *    out = sum over K blocks g of a_s[m,g] * b_s[n/128, g] * partial_g.
+ *  - block scales (sglang PR #44861, duplicate check: it names the block /
+ *    MXFP8 GEMM of PR #42865 without detail; the layout here is the plainest
+ *    one): A carries one scale per row and 128-wide K block, B one per
+ *    128 x 128 block, and out = sum over K blocks g of
+ *    a_s[m,g] * b_s[n/128, g] * partial_g.
  */
 #include <math.h>
 #include <pthread.h>

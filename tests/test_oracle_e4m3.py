@@ -2,7 +2,8 @@
 
 The checks do not reuse the oracle's formulas: decode is pinned by format
 facts and by structure (monotone, symmetric, 254 finite codes); encode is
-pinned by printed values from the pages and by a brute-force nearest-value
+pinned by the tie values printed in sglang PR #33533 (Motivation) and by a
+brute-force nearest-value
 search over the decoded grid, run exhaustively over every fp32 input in the
 range where rounding happens.
 """
