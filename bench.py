@@ -251,10 +251,11 @@ def run_gpu(args, rank, world, local_rank):
     if rank == 0:
         quant_obj = bench_group_quant(torch, fm, synth, dev, flush)
 
-    widened = per_tensor = None
+    widened = per_tensor = determ = None
     if rank == 0:
         widened = bench_widened(torch, fm, synth, dev, flush, work[0])
         per_tensor = bench_per_tensor(torch, fm, dev, flush)
+        determ = bench_deterministic(torch, fm, dev, flush)
 
     # ---- end to end through the C ABI with host buffers
     e2e = None
@@ -263,7 +264,7 @@ def run_gpu(args, rank, world, local_rank):
 
     res = dict(step_ms=tot_step_ms / args.steps, gemm_ms=tot_gemm_ms / args.steps,
                quant_ms=tot_quant_ms / args.steps, wall=wall, step_flops=step_flops,
-               step_quant_bytes=step_quant_bytes, clocks=clocks, quant=quant_obj, e2e=e2e, widened=widened, per_tensor=per_tensor,
+               step_quant_bytes=step_quant_bytes, clocks=clocks, quant=quant_obj, e2e=e2e, widened=widened, per_tensor=per_tensor, determ=determ,
                per_shape_gemm_ms=[x / args.steps for x in per_shape_gemm], launches=2 * len(work) * args.steps)
     return res
 
@@ -405,6 +406,30 @@ def bench_per_tensor(torch, fm, dev, flush, reps=10):
                         "gbs": round(nbytes / (us * 1e-6) / 1e9, 1), "bound": "hbm" if M <= 128 else "tensor"})
             del A, D
         del B
+    return out
+
+
+def bench_deterministic(torch, fm, dev, flush, reps=10):
+    """Cost of the deterministic (batch-invariant) mode on the deterministic
+    configuration's shapes (K = 4096, N in 64, 4096, lda = K + 64, bf16 out with
+    bias): event-timed normal and deterministic launches, L2 flushed before each."""
+    g = torch.Generator(device=dev).manual_seed(12)
+    out = []
+    K = 4096
+    for N in (64, 4096):
+        B = torch.randint(0, 126, (N, K), generator=g, dtype=torch.uint8, device=dev)
+        b_s = torch.rand((N, 1), generator=g, device=dev) * 1e-3
+        bias = (torch.rand((N,), generator=g, device=dev) - 0.5).to(torch.bfloat16)
+        for M in (1, 16, 128, 1024, 4096):
+            A = torch.randint(0, 126, (M, K + 64), generator=g, dtype=torch.uint8, device=dev)
+            a_s = torch.rand((M, 1), generator=g, device=dev) + 0.5
+            D = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            t = {}
+            for det in (False, True):
+                t[det] = _median_us(torch, flush, lambda: fm.fp8_scaled_mm(A, B, a_s, b_s, fm.A_ROW | fm.B_COL, D,
+                                                                           bias=bias, deterministic=det, K=K), reps)
+            out.append({"M": M, "N": N, "K": K, "us": round(t[False], 2), "us_deterministic": round(t[True], 2),
+                        "ratio": round(t[True] / t[False], 3)})
     return out
 
 
@@ -699,6 +724,10 @@ def main():
             v["frac"] = round(v["gbs"] / hbm_peak if v["bound"] == "hbm" else v["tflops"] / fp8_peak, 4)
         line["per_tensor_k4096"] = {"note": "per-tensor scales, L2 flushed before each launch, event-timed; "
                                             "frac of HBM (M <= 128) or of the FP8 peak", "shapes": res["per_tensor"]}
+    if res["determ"]:
+        line["deterministic_cost_k4096"] = {"note": "rowwise scales, bias, lda = K + 64; event-timed normal vs "
+                                                    "deterministic launches, L2 flushed before each",
+                                            "shapes": res["determ"]}
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_rows)
     print(json.dumps(line), flush=True)

@@ -1068,7 +1068,8 @@ int pick_splits(int64_t M, int64_t N, int num_kb, int sms) {
 }
 
 // Shape-keyed tile table.  Deterministic mode picks its tile from N alone, so every M
-// (and every prefix / suffix of the rows) runs the same tile, K order and instruction.
+// (and every prefix / suffix of the rows) runs the same tile, K order and instruction;
+// otherwise the width with the smallest estimated time wins.
 Config pick_config(int64_t M, int64_t N, bool deterministic, bool group_a, int sms) {
   if (group_a) return {kGroupBN, 4, true};
   if (deterministic) {
@@ -1076,10 +1077,24 @@ Config pick_config(int64_t M, int64_t N, bool deterministic, bool group_a, int s
     if (N >= 256) return {128, 6, false};
     return {64, 8, false};
   }
-  const int mblk = ceil_div(M, BM);
-  if (static_cast<int64_t>(mblk) * ceil_div(N, 256) >= sms) return {256, 4, false};
-  if (static_cast<int64_t>(mblk) * ceil_div(N, 128) >= sms) return {128, 6, false};
-  return {64, 8, false};
+  // Estimated time ~ waves x tile width / relative MMA efficiency of that width
+  // (measured on the prefill shapes: BN = 128 runs at 0.6 of BN = 256's rate; BN = 64
+  // lower still), so a partly idle single wave of wide tiles can beat two waves of
+  // narrow ones.
+  const int64_t mblk = ceil_div(M, BM);
+  const Config opts[3] = {{256, 4, false}, {128, 6, false}, {64, 8, false}};
+  const double eff[3] = {1.0, 0.6, 0.33};
+  int best = 0;
+  double best_cost = 0.0;
+  for (int i = 0; i < 3; ++i) {
+    const int64_t tiles = mblk * ceil_div(N, opts[i].bn);
+    const double cost = static_cast<double>((tiles + sms - 1) / sms) * opts[i].bn / eff[i];
+    if (i == 0 || cost < best_cost) {
+      best = i;
+      best_cost = cost;
+    }
+  }
+  return opts[best];
 }
 
 }  // namespace
