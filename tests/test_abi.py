@@ -117,3 +117,21 @@ def test_masked_and_new_entry_validation(L):
     w = (ctypes.c_int64 * 2)(6, 6)
     assert rq(f, f, f, ctypes.cast(w, ctypes.c_void_p), 2, 8, 32, f, None) == -1   # shards past N
     assert rq(f, f, f, ctypes.cast(w, ctypes.c_void_p), 0, 8, 32, f, None) == -1   # no shards
+
+
+def test_plain_c_consumer(L, tmp_path):
+    # the header compiles as C11 and a C program links the library and gets the
+    # documented statuses back (host-side paths only)
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    lib_dir = os.path.join(ROOT, "fp8_scaled_gemm_mm_gb300", "_build")
+    exe = str(tmp_path / "consumer")
+    subprocess.check_call([gcc, "-std=c11", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"),
+                           os.path.join(ROOT, "tests", "c_abi", "consumer.c"), "-L", lib_dir, "-lfp8mm",
+                           "-Wl,-rpath," + lib_dir, "-o", exe])
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert "c consumer ok" in r.stdout
