@@ -484,13 +484,50 @@ def bench_e2e(torch, fm, work, flush, args):
 
 # ---------------------------------------------------- single-kernel cases
 
+def _widened_case(torch, fm, synth, dev, case):
+    """(launch, bytes) of one widened kernel on the workload bench_widened times."""
+    QM, QK = QUANT_M, QUANT_K
+    if case == "quant_masked":
+        E, T, KM = 32, 256, 2048
+        counts = synth.masked_counts(4096, E)
+        xm = synth.quant_input(E * T, 2 * KM, torch.bfloat16, seed=6, device=dev).reshape(E, T, 2 * KM)
+        mm = torch.from_numpy(counts).to(dev)
+        qm = torch.empty((E, T, KM), dtype=torch.uint8, device=dev)
+        sm = torch.empty(fm.masked_scale_shape(E, T, KM, 128, fm.SCALE_UE8M0_PACKED, True), dtype=torch.int32,
+                         device=dev)
+        rows = int(counts.sum())
+        return (lambda: fm.silu_and_mul_masked_post_quant_fp8(xm, mm, qm, sm, 128)), rows * KM * 5 + rows * (KM // 512) * 4
+    if case == "requant":
+        NW, KW = 2 * 14336, 4096
+        w = torch.randint(0, 126, (NW, KW), generator=torch.Generator(device=dev).manual_seed(9), dtype=torch.uint8,
+                          device=dev)
+        w_out = torch.empty_like(w)
+        ss = torch.tensor([0.011, 0.013], dtype=torch.float32, device=dev)
+        return (lambda: fm.requantize_with_max_scale_fp8(w, ss, [14336, 14336], w_out=w_out)), NW * KW * 2
+    x = synth.quant_input(QM, QK, torch.bfloat16, seed=8, device=dev)
+    q = torch.empty((QM, QK), dtype=torch.uint8, device=dev)
+    if case == "static_quant":
+        sc = torch.full((1,), 0.01, dtype=torch.float32, device=dev)
+        return (lambda: fm.static_per_tensor_quant_fp8(x, sc, q)), QM * QK * 3
+    if case == "quant_int8":
+        si = torch.empty(fm.scale_shape(QM, QK, 128, fm.SCALE_FP32, True), dtype=torch.float32, device=dev)
+        qi = q.view(torch.int8)
+        return (lambda: fm.per_token_group_quant_int8(x, qi, si, 128, True)), QM * QK * 3 + si.numel() * 4
+    xs = x[: QM - 192]
+    sp = torch.empty(fm.scale_shape(QM, QK, 128, fm.SCALE_FP32, True), dtype=torch.float32, device=dev)
+    return ((lambda: fm.per_token_group_quant_fp8_row_padded(xs, q, sp, 128)),
+            (QM - 192) * QK * 2 + QM * QK + sp.numel() * 4)
+
+
 def run_kernel_case(args):
     """Launch one kernel on its workload warmup + steps times (for profilers)
     and print its event-timed median.  gemm: a prefill shape (--shape, default
     8320x5376x21504) or --mnk M,K,N, rowwise scales; gemm_block: the same
     shapes with group-128 UE8M0 A scales and 128x128 B block scales; quant / quant_fused:
     group-128 quant of M=8192, K=7168 bf16 with UE8M0 packed column-major
-    scales."""
+    scales; quant_masked: the masked fused quant on the EP decode layout (E=32,
+    T=256, K=2048); quant_int8 / quant_row_padded / static_quant / requant: the
+    widened paths on the workloads the benchmark reports for them."""
     import torch
     import fp8_scaled_gemm_mm_gb300 as fm
     from fp8_scaled_gemm_mm_gb300 import synth
@@ -522,6 +559,8 @@ def run_kernel_case(args):
 
             def launch():
                 fm.fp8_scaled_mm(A, B, a_s, b_s, fm.A_GROUP128_UE8M0 | fm.B_BLOCK128, D)
+    elif args.kernel_case in ("quant_masked", "quant_int8", "quant_row_padded", "static_quant", "requant"):
+        launch, work = _widened_case(torch, fm, synth, dev, args.kernel_case)
     else:
         fuse = args.kernel_case == "quant_fused"
         M, K = QUANT_M, QUANT_K
@@ -625,7 +664,9 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=16, help="oracle rows per shape per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--kernel-case", choices=["gemm", "gemm_block", "quant", "quant_fused"], default=None,
+    ap.add_argument("--kernel-case", choices=["gemm", "gemm_block", "quant", "quant_fused", "quant_masked",
+                                              "quant_int8", "quant_row_padded", "static_quant", "requant"],
+                    default=None,
                     help="run a single kernel on its workload (for profilers) instead of the benchmark")
     ap.add_argument("--shape", type=int, default=0, help="prefill shape index for --kernel-case gemm")
     ap.add_argument("--mnk", default=None, help="M,K,N for --kernel-case gemm instead of a prefill shape")
