@@ -64,11 +64,37 @@ def load_peaks():
     return dict(FALLBACK), "fallback"
 
 
+def _code_only(text):
+    """C/C++ source without comments and blank-line or indentation differences, so
+    that editing a comment does not count as changing a kernel."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c == '"' or c == "'":                       # string / char literal, kept whole
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    lines = (ln.strip() for ln in "".join(out).splitlines())
+    return "\n".join(ln for ln in lines if ln)
+
+
 def source_hash(*rel):
+    """Hash of the code (comments and layout ignored) of the given source files."""
     h = hashlib.sha256()
     for r in rel:
-        with open(os.path.join(ROOT, r), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, r), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

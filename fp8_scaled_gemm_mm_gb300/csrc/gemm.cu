@@ -19,15 +19,23 @@
 // from K so that a group's A panel stays in L2) so that the CTAs running at the
 // same time share A and B panels in L2.
 //
+// The tile width (BN = 256, 128 or 64) is the one with the smallest estimated time,
+// waves x width / the width's relative MMA efficiency.
+//
 // Per-group A scales (one per 128-wide K block, the layout the group quant produces),
 // optionally with 128 x 128 block B scales, run in fp8_gemm_group_kernel: every K
-// block goes to its own TMEM accumulator (a ring of four) and eight epilogue warps
-// promote it, acc += a_s[m, kb] (* b_s[n/128, kb]) * partial_kb, in fp32 registers.
+// block goes to its own TMEM accumulator (128 x 256 tiles, a ring of two) and eight
+// epilogue warps, given the registers of the TMA/MMA warpgroup by setmaxnreg, fold it
+// in: acc += a_s[m, kb] (* b_s[n/128, kb]) * partial_kb, in fp32 registers.
 //
-// Deterministic mode uses one tile shape (BM=128, BN=64, BK=128), one instruction
-// shape and the natural K-block order for every problem, with no split of K, so row
-// m of the result does not depend on M or on the other rows (sglang PR #44861,
-// Modifications: fixed N=64/K=128 reduction tiles, zero-filled K tails).
+// M <= 128 (outside deterministic mode) runs fp8_gemm_swap_splitk_kernel: the weight
+// is the MMA's 128-row operand and K is split over a thread-block cluster whose
+// partials are summed in rank order through distributed shared memory.
+//
+// Deterministic mode picks the tile from N alone, uses one instruction shape and the
+// natural K-block order for every problem, with no split of K, so row m of the result
+// does not depend on M or on the other rows (sglang PR #44861, Modifications: fixed
+// N=64/K=128 reduction tiles, zero-filled K tails).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
