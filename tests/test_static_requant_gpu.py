@@ -42,7 +42,7 @@ def test_static_quant_activations(dt, M, K):
 
 
 @pytest.mark.parametrize("dt", [0, 1])
-@pytest.mark.parametrize("scale", [1.0, 0.0123, 3.0e-5, 7.5, 2.0 ** -20])
+@pytest.mark.parametrize("scale", [1.0, 0.0123, 3.0e-5, 7.5, 2.0 ** -20, 1.0e30, 2.0 ** -130, 0.0, -0.37])
 def test_static_quant_every_16bit_value(dt, scale):
     # every bit pattern of the input type, NaN and infinities included
     _static_case(np.arange(1 << 16, dtype=np.uint32).astype(np.uint16), dt, scale)
