@@ -1,15 +1,19 @@
 /*
  * fp8mm.h -- C ABI of libfp8mm, the GB300 (sm_103a) FP8 linear-layer hot path.
  *
- * Two operations, both asynchronous on the caller's CUDA stream:
+ * Two operations and their variants, all asynchronous on the caller's CUDA
+ * stream:
  *
- *  1. per_token_group_quant_fp8 (+ a topk scatter variant): bf16/fp16
- *     activations -> E4M3FN codes + fp32 / UE8M0 scales, the producer of the
- *     GEMM's A operand.
- *     Defined by sglang PR #33533 "[JIT] per_token_group_quant: fix the fp16
- *     UE8M0 multiplier overflow, 1.23x on the fused EP-MoE path, unify the
- *     scale allocation" (Motivation; Modifications 1-3; second commit note
- *     for the scatter).
+ *  1. per_token_group_quant_fp8: bf16/fp16 activations -> E4M3FN codes +
+ *     fp32 / UE8M0 scales, the producer of the GEMM's A operand; variants:
+ *     topk scatter, the masked expert-major layout with fused SiLU*up, int8
+ *     output, row-padded outputs.  Defined by sglang PR #33533 "[JIT]
+ *     per_token_group_quant: fix the fp16 UE8M0 multiplier overflow, 1.23x on
+ *     the fused EP-MoE path, unify the scale allocation" (Motivation;
+ *     Modifications 1-3; commit notes for the scatter and the entry points).
+ *     Static per-tensor activation quant and the requantization of a fused
+ *     weight's per-shard scales to their maximum follow the prhub summary of
+ *     sglang PR #33148 (Key source snippets).
  *
  *  2. fp8_scaled_mm: D = out_dtype(a_scale * b_scale * A B^T (+ bias)) with
  *     E4M3FN A [M,K] and B [N,K] (both K-major) and fp32 scales.
