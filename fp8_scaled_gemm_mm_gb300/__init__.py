@@ -94,11 +94,25 @@ def _stream(stream):
     return int(stream)
 
 
-def _ptr(t):
+def _ptr(t, name="tensor", row_strided=False):
+    """Device address of t for the C ABI.  The entry points take a base pointer
+    and dense extents (the GEMM operands also a row stride), so a tensor has to
+    live on a CUDA device and be contiguous; a 2-D GEMM operand only needs unit
+    stride along its last dimension.  A host tensor's address would be read as
+    a device address, and a strided view would be read as if it were dense, so
+    both are refused here.  Plain ints pass through as raw device addresses."""
     if t is None:
         return None
     if isinstance(t, int):
         return t
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor, got one on {t.device}")
+    if t.numel() > 0:
+        if row_strided and t.dim() == 2:
+            if t.stride(1) != 1:
+                raise ValueError(f"{name} needs unit stride along its last dimension, got strides {t.stride()}")
+        elif not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous, got strides {t.stride()} for shape {tuple(t.shape)}")
     return t.data_ptr()
 
 
@@ -141,8 +155,9 @@ def per_token_group_quant_fp8(x, q, s, group: int, ue8m0: int = SCALE_FP32, scal
         M = x.shape[0]
     if K is None:
         K = x.shape[1] // 2 if fuse_silu_mul else x.shape[1]
-    st = lib().per_token_group_quant_fp8(_ptr(x), x_dtype, _ptr(q), _ptr(s), M, K, group, int(ue8m0),
-                                         int(bool(scale_colmajor)), int(bool(fuse_silu_mul)), _stream(stream))
+    st = lib().per_token_group_quant_fp8(_ptr(x, "x"), x_dtype, _ptr(q, "q"), _ptr(s, "s"), M, K, group,
+                                         int(ue8m0), int(bool(scale_colmajor)), int(bool(fuse_silu_mul)),
+                                         _stream(stream))
     _check(st, "per_token_group_quant_fp8")
 
 
@@ -151,8 +166,9 @@ def per_token_group_quant_int8(x, q, s, group: int, scale_colmajor: bool = False
     """int8 group quant: x [M, K] (or [M, 2K] fused) -> q int8 [M, K], s fp32."""
     M = x.shape[0]
     K = x.shape[1] // 2 if fuse_silu_mul else x.shape[1]
-    st = lib().per_token_group_quant_int8(_ptr(x), _DTYPE_CODE[x.dtype], _ptr(q), _ptr(s), M, K, group,
-                                          int(bool(scale_colmajor)), int(bool(fuse_silu_mul)), _stream(stream))
+    st = lib().per_token_group_quant_int8(_ptr(x, "x"), _DTYPE_CODE[x.dtype], _ptr(q, "q"), _ptr(s, "s"), M, K,
+                                          group, int(bool(scale_colmajor)), int(bool(fuse_silu_mul)),
+                                          _stream(stream))
     _check(st, "per_token_group_quant_int8")
 
 
@@ -161,9 +177,9 @@ def per_token_group_quant_fp8_row_padded(x, q, s, group: int, ue8m0: int = SCALE
     """Group quant of x [M, K] into q [M_pad, K] / s sized for M_pad = q.shape[0]
     rows; rows M .. M_pad-1 are zeroed."""
     M, K = x.shape
-    st = lib().per_token_group_quant_fp8_row_padded(_ptr(x), _DTYPE_CODE[x.dtype], _ptr(q), _ptr(s), M, q.shape[0],
-                                                    K, group, int(ue8m0), int(bool(scale_colmajor)),
-                                                    _stream(stream))
+    st = lib().per_token_group_quant_fp8_row_padded(_ptr(x, "x"), _DTYPE_CODE[x.dtype], _ptr(q, "q"),
+                                                    _ptr(s, "s"), M, q.shape[0], K, group, int(ue8m0),
+                                                    int(bool(scale_colmajor)), _stream(stream))
     _check(st, "per_token_group_quant_fp8_row_padded")
 
 
@@ -179,9 +195,9 @@ def per_token_group_quant_fp8_scatter(x, dst_row, q, s, group: int, ue8m0: int =
         topk = dst_row.shape[1]
     if num_dst_rows is None:
         num_dst_rows = q.shape[0]
-    st = lib().per_token_group_quant_fp8_scatter(_ptr(x), x_dtype, _ptr(dst_row), topk, num_dst_rows, _ptr(q),
-                                                 _ptr(s), M, K, group, int(ue8m0), int(bool(scale_colmajor)),
-                                                 _stream(stream))
+    st = lib().per_token_group_quant_fp8_scatter(_ptr(x, "x"), x_dtype, _ptr(dst_row, "dst_row"), topk,
+                                                 num_dst_rows, _ptr(q, "q"), _ptr(s, "s"), M, K, group, int(ue8m0),
+                                                 int(bool(scale_colmajor)), _stream(stream))
     _check(st, "per_token_group_quant_fp8_scatter")
 
 
@@ -198,16 +214,16 @@ def silu_and_mul_masked_post_quant_fp8(x, masked_m, q, s, group: int, ue8m0: int
                                        scale_colmajor: bool = True, stream=None):
     """x [E, T, 2K] -> q [E, T, K] and s for the first masked_m[e] rows of each expert."""
     E, T, K2 = x.shape
-    st = lib().silu_and_mul_masked_post_quant_fp8(_ptr(x), _DTYPE_CODE[x.dtype], _ptr(masked_m), E, T, K2 // 2,
-                                                  _ptr(q), _ptr(s), group, int(ue8m0), int(bool(scale_colmajor)),
-                                                  _stream(stream))
+    st = lib().silu_and_mul_masked_post_quant_fp8(_ptr(x, "x"), _DTYPE_CODE[x.dtype], _ptr(masked_m, "masked_m"),
+                                                  E, T, K2 // 2, _ptr(q, "q"), _ptr(s, "s"), group, int(ue8m0),
+                                                  int(bool(scale_colmajor)), _stream(stream))
     _check(st, "silu_and_mul_masked_post_quant_fp8")
 
 
 def static_per_tensor_quant_fp8(x, scale, q, stream=None):
     """q = E4M3(x / scale[0]) elementwise (static activation scale)."""
-    st = lib().static_per_tensor_quant_fp8(_ptr(x), _DTYPE_CODE[x.dtype], _ptr(scale), _ptr(q), x.numel(),
-                                           _stream(stream))
+    st = lib().static_per_tensor_quant_fp8(_ptr(x, "x"), _DTYPE_CODE[x.dtype], _ptr(scale, "scale"), _ptr(q, "q"),
+                                           x.numel(), _stream(stream))
     _check(st, "static_per_tensor_quant_fp8")
 
 
@@ -219,9 +235,9 @@ def requantize_with_max_scale_fp8(w, shard_scales, logical_widths, w_out=None, m
     if max_scale_out is None:
         max_scale_out = torch.empty(1, dtype=torch.float32, device=w.device)
     widths = (ctypes.c_int64 * len(logical_widths))(*[int(v) for v in logical_widths])
-    st = lib().requantize_with_max_scale_fp8(_ptr(w), _ptr(w_out), _ptr(shard_scales),
+    st = lib().requantize_with_max_scale_fp8(_ptr(w, "w"), _ptr(w_out, "w_out"), _ptr(shard_scales, "shard_scales"),
                                              ctypes.cast(widths, ctypes.c_void_p), len(logical_widths), N, K,
-                                             _ptr(max_scale_out), _stream(stream))
+                                             _ptr(max_scale_out, "max_scale_out"), _stream(stream))
     _check(st, "requantize_with_max_scale_fp8")
     return w_out, max_scale_out
 
@@ -245,8 +261,9 @@ def fp8_scaled_mm(A, B, a_scale, b_scale, scale_mode: int, out, bias=None, deter
     if ldb is None:
         ldb = B.stride(0) if B.dim() == 2 else K
     out_dtype = _DTYPE_CODE[out.dtype] if isinstance(out, torch.Tensor) else 0
-    st = lib().fp8_scaled_mm(_ptr(A), _ptr(B), _ptr(a_scale), _ptr(b_scale), int(scale_mode), _ptr(bias),
-                             _ptr(out), out_dtype, M, N, K, lda, ldb, int(bool(deterministic)), _stream(stream))
+    st = lib().fp8_scaled_mm(_ptr(A, "A", True), _ptr(B, "B", True), _ptr(a_scale, "a_scale"),
+                             _ptr(b_scale, "b_scale"), int(scale_mode), _ptr(bias, "bias"), _ptr(out, "out"),
+                             out_dtype, M, N, K, lda, ldb, int(bool(deterministic)), _stream(stream))
     _check(st, "fp8_scaled_mm")
 
 
@@ -259,7 +276,7 @@ def get_device_status(device: int = -1, clear: bool = True) -> int:
 def selftest_scale_math(bits_lo: int, bits_hi: int, counters, stream=None):
     """Compare the quant kernels' scale arithmetic with IEEE division over a range
     of fp32 bit patterns; adds mismatch counts to counters (int64 [3], device)."""
-    _check(lib().fp8mm_selftest_scale_math(int(bits_lo), int(bits_hi), _ptr(counters), _stream(stream)),
+    _check(lib().fp8mm_selftest_scale_math(int(bits_lo), int(bits_hi), _ptr(counters, "counters"), _stream(stream)),
            "fp8mm_selftest_scale_math")
 
 

@@ -135,3 +135,21 @@ def test_plain_c_consumer(L, tmp_path):
     r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
     assert r.returncode == 0, r.stdout + r.stderr
     assert "c consumer ok" in r.stdout
+
+
+def test_binding_refuses_host_tensors(L):
+    # a host tensor's address must never reach a kernel: the binding raises
+    # before it calls into the library
+    import torch
+    import fp8_scaled_gemm_mm_gb300 as fm
+    x = torch.zeros((4, 128), dtype=torch.bfloat16)
+    q = torch.zeros((4, 128), dtype=torch.uint8)
+    s = torch.zeros((4, 1), dtype=torch.float32)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        fm.per_token_group_quant_fp8(x, q, s, 128)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        fm.static_per_tensor_quant_fp8(x, torch.ones(1), q)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        fm.fp8_scaled_mm(q, q, s, s, fm.A_ROW | fm.B_COL, x)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        fm.requantize_with_max_scale_fp8(q, torch.ones(2), [2, 2], max_scale_out=torch.ones(1))

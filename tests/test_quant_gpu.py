@@ -258,3 +258,27 @@ def test_masked_silu_quant_edges():
     # counts beyond the capacity are clamped and reported
     masked = np.array([5, 120, 0, 100], np.int32)
     assert _masked_case(4, 100, 512, masked, seed=83) == fm.EINVAL
+
+
+def test_binding_refuses_strided_views():
+    # the entry points read dense extents from a base pointer, so a strided view
+    # would be read as if it were dense: the binding refuses it instead
+    dev = require_gpu()
+    x = torch.zeros((256, 128), dtype=torch.bfloat16, device=dev)
+    q, s = fm.alloc_group_quant_outputs(128, 256, 128, fm.SCALE_FP32, False, device=dev)
+    with pytest.raises(ValueError, match="contiguous"):
+        fm.per_token_group_quant_fp8(x.t(), q, s, 128)
+    w = torch.zeros((256, 256), dtype=torch.uint8, device=dev)
+    a_s = torch.ones((128, 1), dtype=torch.float32, device=dev)
+    w_s = torch.ones((256, 1), dtype=torch.float32, device=dev)
+    out = torch.empty((128, 256), dtype=torch.bfloat16, device=dev)
+    with pytest.raises(ValueError, match="unit stride"):
+        fm.fp8_scaled_mm(q, w.t(), a_s, w_s, fm.A_ROW | fm.B_COL, out)
+    out_t = torch.empty((256, 128), dtype=torch.bfloat16, device=dev).t()
+    with pytest.raises(ValueError, match="contiguous"):
+        fm.fp8_scaled_mm(q, w, a_s, w_s, fm.A_ROW | fm.B_COL, out_t)
+    # row-strided operand views (row stride 256 > K = 128) are the supported way to pass a slice
+    fm.fp8_scaled_mm(w[:128, :128], w[:, :128], a_s, w_s, fm.A_ROW | fm.B_COL, out)
+    torch.cuda.synchronize()
+    assert fm.get_device_status() == 0
+    assert not out.isnan().any()
