@@ -267,6 +267,12 @@ def test_static_quant_pins():
     # beyond the range the codes saturate to +-448
     q = oracle.static_quant(x, 0, 1e-3)
     assert np.all(np.abs(oracle.e4m3_decode(q)) <= 448) and np.any((q & 0x7F) == 0x7E)
+    # an IEEE divide, not a multiply by the reciprocal: 87.5 / 7 = 12.5 exactly, the
+    # midpoint of 12 (0x54) and 13 (0x55), which goes to the even code 0x54;
+    # fl32(1/7) = (1/7)(1 + 4.47e-8) would give 87.5 * fl32(1/7) = 12.50000056,
+    # rounded to 12.5 + 2^-20 and so to 13
+    xb = np.array([0x42AF, 0xC2AF], np.uint16)                  # bf16 87.5, -87.5
+    assert list(oracle.static_quant(xb, 0, 7.0)) == [0x54, 0xD4]
 
 
 def test_requantize_with_max_scale_pins():
@@ -283,6 +289,15 @@ def test_requantize_with_max_scale_pins():
     assert np.array_equal(out[:32], w[:32]) and np.array_equal(out[80:], w[80:])
     mid = oracle.e4m3_decode(w[32:80]) / 4
     assert np.array_equal(out[32:80], oracle.e4m3_encode(mid.astype(np.float32)))
+    # the dequantized weight is fp32: code 0x11 is d = 9*2^-8 and the shard scale
+    # s = 0x4089C71C = 2257351*2^-19, so d*s = 20316159*2^-27, a 25-bit odd
+    # significand whose rounding to fp32 is a tie, resolved to the even 20316160*2^-27
+    # = 155*2^-10.  Divided by s_max = 5 that is 31*2^-10 exactly, the midpoint of
+    # 15*2^-9 (0x0F) and 16*2^-9 (0x10): the even code 0x10.  (Without the fp32
+    # rounding of d*s the quotient lies just below the midpoint: 0x0F.)
+    s_i = np.array([0x4089C71C], np.uint32).view(np.float32)[0]
+    out, smax = oracle.requantize_with_max_scale(np.array([[0x11], [0x11]], np.uint8), [s_i, 5.0], [1, 1])
+    assert smax == np.float32(5.0) and out[0, 0] == 0x10
 
 
 def test_int8_encode_pins():
