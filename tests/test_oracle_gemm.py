@@ -36,6 +36,10 @@ def test_accumulation_is_exact_int64():
     acc = _int_form(A) @ _int_form(B).T            # exact in int64
     assert np.array_equal(exact, acc.astype(np.float64) / 2.0 ** 18)
     assert np.array_equal(out, oracle.round_bf16(acc / 2.0 ** 18))
+    # scalar scales that are powers of two scale the exact sum exactly
+    _, e2, _ = oracle.gemm(A, B, np.float32(2.0 ** -3), np.float32(2.0 ** 5), oracle.A_TENSOR, oracle.B_TENSOR,
+                           want_exact=True)
+    assert np.array_equal(e2, acc.astype(np.float64) / 2.0 ** 16)
 
 
 def test_extreme_accumulation_k28672():

@@ -244,12 +244,12 @@ def test_masked_counts_sum_to_routed_tokens():
 def test_block_quant_is_groupwise_per_block():
     # each 128 x 128 block: absmax/448 scale, its largest element at +-448, and the
     # same codes as the group quant of the block taken as one row
-    w = synth.to_bits(synth.normal((200, 256), 0.02, seed=91))
+    w = synth.to_bits(synth.normal((200, 384), 0.02, seed=91))
     q, s = oracle.quantize_blocks(w)
-    assert q.shape == (200, 256) and s.shape == (2, 2)
+    assert q.shape == (200, 384) and s.shape == (2, 3)
     v = oracle.bf16_bits_to_f64(w)
     for i in range(2):
-        for j in range(2):
+        for j in range(3):
             blk = v[i * 128:(i + 1) * 128, j * 128:(j + 1) * 128]
             a = np.abs(blk).max()
             assert abs(s[i, j] - a / 448) <= a / 448 * 2.0 ** -23
@@ -273,13 +273,15 @@ def test_static_quant_pins():
     # rounded to 12.5 + 2^-20 and so to 13
     xb = np.array([0x42AF, 0xC2AF], np.uint16)                  # bf16 87.5, -87.5
     assert list(oracle.static_quant(xb, 0, 7.0)) == [0x54, 0xD4]
+    xh = np.array([0x5578, 0xD578], np.uint16)                  # fp16 87.5, -87.5
+    assert list(oracle.static_quant(xh, 1, 7.0)) == [0x54, 0xD4]
 
 
 def test_requantize_with_max_scale_pins():
     rng = np.random.default_rng(93)
-    w = rng.integers(0, 256, size=(96, 64), dtype=np.uint8)
+    w = rng.integers(0, 256, size=(100, 64), dtype=np.uint8)
     w[(w & 0x7F) == 0x7F] = 0x30
-    widths = [32, 48, 16]
+    widths = [32, 48, 16]                   # rows 96..99 lie past the shards and are copied
     # equal shard scales: nothing changes
     out, smax = oracle.requantize_with_max_scale(w, [0.5, 0.5, 0.5], widths)
     assert np.array_equal(out, w) and smax == np.float32(0.5)
@@ -310,6 +312,19 @@ def test_int8_encode_pins():
     r = (np.random.default_rng(94).standard_normal(20000) * 60).astype(np.float32)
     r[::7] = np.round(r[::7]) + 0.5
     assert np.array_equal(oracle.i8_encode(r), np.clip(np.rint(r), -128, 127).astype(np.int8))
+
+
+def test_int8_multiplier_is_an_ieee_quotient():
+    # a = 143/64: fl32(127/a) = 14900045*2^-18, and a times it is 127 + 1.8e-7, which
+    # rounds to 127 (code 127).  v = a/2 = 143/128 gives v*mult = 63.5 + 9e-8 exactly,
+    # which rounds to 63.5, a tie that goes to the even 64.  (The reciprocal of the
+    # stored scale fl32(a/127) = 0x3C902041 is one ulp smaller and would give
+    # 63.499996 -> 63.)
+    x = np.zeros((1, 128), np.uint16)
+    x[0, :3] = [0x400F, 0x3F8F, 0xBF8F]                     # bf16 143/64, 143/128, -143/128
+    q, s = oracle.group_quant_int8(x, 0, 128)
+    assert list(q[0, :3]) == [127, 64, -64] and not q[0, 3:].any()
+    assert s.view(np.uint32)[0, 0] == 0x3C902041
 
 
 def test_int8_group_quant_properties():
