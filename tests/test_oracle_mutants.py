@@ -80,6 +80,36 @@ MUTANTS = [
        "if (j->bias) val += (double)bf16_to_float(j->bias[n]) * bs;", 1)]),
     ("gemm accumulates in fp32", C_SRC, [("double p = lut[a[k]] * lut[b[k]];\n          acc += p;",
                                           "double p = lut[a[k]] * lut[b[k]];\n          acc = (float)(acc + p);", 1)]),
+    ("exp overflow threshold too low", C_SRC, [("if (x > 89.0f) return INFINITY;", "if (x > 80.0f) return INFINITY;", 1)]),
+    ("exp 2^n split loses a factor two", C_SRC, [("int n2 = ni - n1;", "int n2 = ni - n1 - (ni < 0);", 1)]),
+    ("silu denominator 1 - exp(-g)", C_SRC, [("float d = 1.0f + e;", "float d = 1.0f - e;", 1)]),
+    ("ue8m0 byte one below the scale's exponent", C_SRC, [("eb = (uint8_t)ex;", "eb = (uint8_t)(ex - 1);", 1)]),
+    ("e4m3 subnormal code off by one", C_SRC,
+     [("return (uint8_t)(r / ldexp(1.0, -9)); /* subnormal: m */", "return (uint8_t)(r / ldexp(1.0, -9) - 1);", 1)]),
+    ("bf16 overflow one binade late", C_SRC,
+     [("if (r >= ldexp(1.0, emax + 1)) return INFINITY;", "if (r >= ldexp(1.0, emax + 2)) return INFINITY;", 1)]),
+    ("fp16 decode subnormals one binade low", C_SRC,
+     [("else if (e == 0) v = ldexp((double)m, -24);", "else if (e == 0) v = ldexp((double)m, -25);", 1)]),
+    ("int8 fused path with gate and up swapped", C_SRC,
+     [("v[i] = silu_f32(load_x(x, x_dtype, m * ldx + k)) * load_x(x, x_dtype, m * ldx + K + k);",
+       "v[i] = silu_f32(load_x(x, x_dtype, m * ldx + K + k)) * load_x(x, x_dtype, m * ldx + k);", 1)]),
+    ("int8 multiplier as the reciprocal of the scale", C_SRC,
+     [("float mult = 127.0f / a;", "float mult = 1.0f / (a / 127.0f);", 1)]),
+    ("gemm column-major group scales read row-major", C_SRC,
+     [("case 3: return (double)j->a_scale[g * j->a_ld + m];", "case 3: return (double)j->a_scale[g];", 1)]),
+    ("gemm per-tensor B scale ignored", C_SRC,
+     [("double bs = j->b_mode == 0 ? (double)j->b_scale[0]", "double bs = j->b_mode == 0 ? 1.0", 1)]),
+    ("row-major ue8m0 words laid out column-major", PY_SRC,
+     [("        out = np.zeros((R, W), np.int32)\n        for m, d in pairs:\n            out[d] = words[m]",
+       "        out = np.zeros((R, W), np.int32)\n        for m, d in pairs:\n            out[d] = words[m][::-1]", 1)]),
+    ("requant zeroes the rows past the shards", PY_SRC, [("out[start:] = w[start:]", "out[start:] = 0", 1)]),
+    ("static quant reads fp16 as bf16", PY_SRC,
+     [("v = (bf16_bits_to_f64(x) if x_dtype == 0 else fp16_bits_to_f64(x)).astype(np.float32)",
+       "v = bf16_bits_to_f64(x).astype(np.float32)", 1)]),
+    ("block quant scales transposed", PY_SRC, [("s[i, j] = sb[0, 0]", "s[j % nb, i % kb] = sb[0, 0]", 1)]),
+    ("scatter codes written to the first destination only", PY_SRC,
+     [("        for d in dst[m]:\n            if d >= 0:\n                qd[d] = q[m]",
+       "        for d in dst[m][:1]:\n            if d >= 0:\n                qd[d] = q[m]", 1)]),
     # layouts and the Python-level paths
     ("column-major scales without the pad-4 stride", PY_SRC,
      [("out = np.zeros((G, pad4(R)), np.float32)", "out = np.zeros((G, R), np.float32)", 1)]),
