@@ -54,13 +54,20 @@ def build(force: bool = False, verbose: bool = False) -> str:
         obj = os.path.join(OUT_DIR, unit.replace(".cu", ".o"))
         objs.append(obj)
         if force or _stale(obj, [src] + hdrs + [__file__]):
-            cmd = [nvcc, *ARCH, *COMMON, *extra, "-c", src, "-o", obj]
+            # each object is written under a private name and moved into place, so
+            # that two builds running at once never link a half-written object
+            cmd = [nvcc, *ARCH, *COMMON, *extra, "-c", src, "-o", obj + f".tmp{os.getpid()}"]
             if verbose:
                 cmd.insert(1, "-Xptxas=-v")
-            jobs.append(cmd)
+            jobs.append((cmd, obj))
 
-    def run(cmd):
+    def run(job):
+        cmd, obj = job
         r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode == 0:
+            os.replace(cmd[-1], obj)
+        elif os.path.exists(cmd[-1]):
+            os.remove(cmd[-1])
         return cmd, r
 
     if jobs:
