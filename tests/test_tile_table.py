@@ -1,0 +1,91 @@
+"""The GEMM planner's host logic, on the CPU: the shape-keyed tile table and the
+split count of the small-M path (tests/c_abi/tile_table.cu compiles the
+library's sources into a host program that answers plan queries; no kernel
+runs).
+
+Checked: deterministic mode picks its tile from N alone, so every M (every
+prefix or suffix of the rows) runs the same tile and reduction (sglang PR #44861,
+Modifications: fixed reduction tiles); group scales always take the group
+kernel's tile; the widest tile wins wherever it fills the machine; the split
+count keeps each of its stated limits and is the largest that does."""
+import os
+import shutil
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+BK = 128
+SMS = 152
+
+
+@pytest.fixture(scope="module")
+def plan(tmp_path_factory):
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    if not os.path.exists(nvcc):
+        pytest.skip("nvcc is needed to build the planner probe")
+    exe = str(tmp_path_factory.mktemp("tile_table") / "tile_table")
+    # device code to PTX only (no ptxas): the probe calls host functions alone
+    subprocess.check_call([nvcc, "-gencode", "arch=compute_103a,code=compute_103a", "-std=c++17",
+                           "--expt-relaxed-constexpr", "-w", "-I", os.path.join(ROOT, "include"), "-o", exe,
+                           os.path.join(ROOT, "tests", "c_abi", "tile_table.cu")])
+
+    def ask(lines):
+        r = subprocess.run([exe], input="\n".join(lines) + "\n", capture_output=True, text=True, check=True)
+        return [tuple(int(v) for v in ln.split()) for ln in r.stdout.strip().splitlines()]
+    return ask
+
+
+def _configs(plan, shapes, det=0, group=0, sms=SMS):
+    return plan([f"config {M} {N} {det} {group} {sms}" for M, N in shapes])
+
+
+def test_deterministic_tile_depends_on_n_only(plan):
+    Ms = [1, 2, 7, 16, 37, 64, 100, 101, 128, 129, 1000, 4096, 23216]
+    for N in (64, 128, 256, 1024, 4096, 14336, 28672):
+        got = set(_configs(plan, [(M, N) for M in Ms], det=1))
+        assert len(got) == 1, (N, got)
+        bn, _ = got.pop()
+        assert bn in (64, 128, 256)
+    # and it does not depend on the machine size either
+    assert _configs(plan, [(512, 4096)], det=1, sms=148) == _configs(plan, [(512, 4096)], det=1, sms=SMS)
+
+
+def test_group_scales_take_the_group_tile(plan):
+    got = set(_configs(plan, [(M, N) for M in (1, 64, 8320) for N in (256, 5376, 28672)], group=1))
+    assert got == {(256, 4)}
+
+
+def test_prefill_shapes_take_the_widest_tile(plan):
+    # the five prefill shapes fill every wave of 128 x 256 tiles almost exactly
+    shapes = [(8320, 21504), (8320, 14336), (23216, 28672), (15760, 28672), (8320, 5376)]
+    assert all(bn == 256 for bn, _ in _configs(plan, shapes))
+
+
+def test_narrow_tiles_only_when_they_save_a_wave(plan):
+    # a narrower tile is chosen only if it needs fewer waves than 256-wide tiles, or if
+    # the 256-wide tiles fit in one partly idle wave (narrower ones then use more SMs)
+    for M in (256, 384, 1024, 2048):
+        for N in (512, 1024, 1536, 2048, 4096):
+            (bn, _), = _configs(plan, [(M, N)])
+            if bn != 256:
+                mblk = -(-M // 128)
+                waves = lambda w: -(-mblk * -(-N // w) // SMS)
+                assert waves(bn) < waves(256) or waves(256) == 1, (M, N, bn)
+
+
+def test_split_count_limits_and_maximality(plan):
+    cases = [(M, N, kb) for M in (1, 8, 16, 17, 32, 33, 64, 65, 100, 128) for N in (256, 1024, 4096, 14336, 28672)
+             for kb in (1, 2, 3, 8, 32, 112)]
+    got = plan([f"splits {M} {N} {kb} {SMS}" for M, N, kb in cases])
+
+    def limits_ok(M, N, kb, s):
+        tiles = -(-N // 128) * -(-M // 128)
+        bt = 16 if M <= 16 else 32 if M <= 32 else 64 if M <= 64 else 128
+        return (s <= 8 and s * 2 <= kb and tiles * s <= 2 * SMS   # cluster size, 2 K blocks a slice, residency
+                and s <= kb * BK // (16 * bt))                   # partials below half the weight slice
+    for (M, N, kb), (s,) in zip(cases, got):
+        assert s >= 1
+        if s > 1:
+            assert limits_ok(M, N, kb, s), (M, N, kb, s)
+        assert not limits_ok(M, N, kb, s + 1), (M, N, kb, s)   # the largest count that keeps them
