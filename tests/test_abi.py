@@ -153,3 +153,86 @@ def test_binding_refuses_host_tensors(L):
         fm.fp8_scaled_mm(q, q, s, s, fm.A_ROW | fm.B_COL, x)
     with pytest.raises(ValueError, match="CUDA tensor"):
         fm.requantize_with_max_scale_fp8(q, torch.ones(2), [2, 2], max_scale_out=torch.ones(1))
+
+
+def test_gemm_validation_fuzz(L):
+    # Random argument sets, each breaking at least one documented rule (or empty):
+    # every one must come back as EINVAL / EALIGN (or OK for an empty problem) with
+    # nothing launched.  Runs only where no GPU is present, so that a validation
+    # bug could never send the fake pointers to a kernel.
+    import random
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("host-only check: run without a GPU")
+    g = L.fp8_scaled_mm
+    rng = random.Random(7)
+    base = 1 << 24
+    big = 1 << 31
+    checked = 0
+    while checked < 3000:
+        M = rng.choice([-3, 0, 1, 17, 128, 129, 4096, big])
+        N = rng.choice([-1, 0, 8, 12, 256, 4096, big])
+        K = rng.choice([-16, 0, 8, 16, 72, 80, 128, 512, big])
+        lda = max(K, 0) + rng.choice([-16, 0, 0, 8, 16, 64])
+        ldb = max(K, 0) + rng.choice([-16, 0, 0, 8, 16])
+        a_mode, b_mode = rng.choice([0, 1, 2, 3, 4, 5]), rng.choice([0, 1, 2, 3])
+        extra = rng.choice([0, 0, 0, 0x100])
+        od = rng.choice([0, 1, 1, 2])
+        ptrs = [base + (i << 40) + rng.choice([0, 0, 0, 2, 4, 8]) for i in range(5)]
+        if rng.random() < 0.1:
+            ptrs[rng.randrange(5)] = None
+        A, B, a_s, b_s, out = ptrs
+        bias = rng.choice([None, base + (6 << 40), base + (6 << 40) + 1])
+        group = a_mode in (2, 3, 4)
+        rules_broken = (M < 0 or N < 0 or a_mode > 4 or b_mode > 2 or extra or (b_mode == 2 and not group)
+                        or od not in (0, 1) or max(M, N, K) > big - 1 or K <= 0 or K % 16 or lda < K or ldb < K
+                        or lda % 16 or ldb % 16 or N % 8 or (group and K % 128))
+        empty = M == 0 or N == 0
+        if not rules_broken and not empty:
+            rules_broken = (None in (A, B, a_s, b_s, out) or any(p % 16 for p in (A, B, out))
+                            or a_s % 4 or b_s % 4 or (bias is not None and bias % 2))
+        if not rules_broken and not empty:
+            continue                      # a valid request would try to launch: not sent
+        st = g(A, B, a_s, b_s, a_mode | (b_mode << 4) | extra, bias, out, od, M, N, K, lda, ldb, 0, None)
+        if rules_broken:
+            assert st in (-1, -2), (st, M, N, K, lda, ldb, a_mode, b_mode, extra, od, ptrs, bias)
+        else:
+            assert st == 0, (st, M, N, K)
+        checked += 1
+
+
+def test_quant_validation_fuzz(L):
+    # As for the GEMM: requests that break a documented rule (or are empty) only,
+    # never sent where a GPU is present.
+    import random
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("host-only check: run without a GPU")
+    q = L.per_token_group_quant_fp8
+    rng = random.Random(11)
+    base = 1 << 24
+    checked = 0
+    while checked < 3000:
+        M = rng.choice([-2, 0, 1, 33, 8192, 1 << 31])
+        K = rng.choice([-128, 0, 8, 16, 96, 128, 2048, 7168, 2048 + 64])
+        group = rng.choice([16, 32, 64, 96, 128, 256, K])
+        dt = rng.choice([0, 1, 1, 2])
+        fmt = rng.choice([-1, 0, 1, 2, 3])
+        cm, fuse = rng.randrange(2), rng.randrange(2)
+        ptrs = [base + (i << 40) + rng.choice([0, 0, 0, 2, 4, 8]) for i in range(3)]
+        if rng.random() < 0.1:
+            ptrs[rng.randrange(3)] = None
+        x, qq, s = ptrs
+        rules_broken = (M < 0 or K <= 0 or dt not in (0, 1) or fmt not in (0, 1, 2)
+                        or group not in (32, 64, 128, K) or group <= 0 or K % 16 or K % group)
+        empty = M == 0
+        if not rules_broken and not empty:
+            rules_broken = (M > (1 << 31) - 1 or None in ptrs or x % 16 or qq % 16 or s % 4)
+        if not rules_broken and not empty:
+            continue
+        st = q(x, dt, qq, s, M, K, group, fmt, cm, fuse, None)
+        if rules_broken:
+            assert st in (-1, -2), (st, M, K, group, dt, fmt, ptrs)
+        else:
+            assert st == 0, (st, M, K, group)
+        checked += 1
