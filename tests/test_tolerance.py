@@ -64,3 +64,18 @@ def test_rejects_a_wrong_kernel(case, mistake):
         got = oracle.round_bf16(c["exact"] + oracle.bf16_bits_to_f64(c["bias"])[None, :])
     with pytest.raises(AssertionError):
         check_gemm(got, c["exact"], c["sumabs"], K)
+
+
+@pytest.mark.parametrize("chunk", [128, 32])
+def test_accepts_an_fp32_kernel_at_the_largest_k(chunk):
+    # K = 14336 (the down projection of the prefill shapes): an fp32 accumulation in
+    # K chunks still passes, the largest-K case of the accumulation-error allowance
+    m, n, k = 16, 64, 14336
+    A, a_s, B, b_s = gemm_inputs(m, n, k, "row", "col", seed_a=31, seed_b=32)
+    _, exact, sumabs = oracle.gemm(A, B, a_s, b_s, oracle.A_ROW, oracle.B_COL, want_exact=True)
+    da, db = oracle.e4m3_decode(A).astype(np.float32), oracle.e4m3_decode(B).astype(np.float32)
+    acc = np.zeros((m, n), np.float32)
+    for k0 in range(0, k, chunk):
+        acc = (acc + da[:, k0:k0 + chunk] @ db[:, k0:k0 + chunk].T).astype(np.float32)
+    v = (acc * np.asarray(a_s, np.float32).reshape(m, 1) * np.asarray(b_s, np.float32).reshape(1, n))
+    check_gemm(oracle.round_bf16(v.astype(np.float32).astype(np.float64)), exact, sumabs, k)
