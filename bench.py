@@ -47,6 +47,15 @@ FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
 L2_FLUSH_BYTES = 512 << 20
 
 
+def workload_config(world):
+    """The `config` object of the JSON line; the same for both arms."""
+    return {"workload": "large rowwise-scaled FP8 prefill GEMMs (5 shapes) + per-token activation quant",
+            "shapes_MxKxN": [list(s) for s in SHAPES], "out": "bf16", "scales": "fp32 per-row x per-col",
+            "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write, then {L2_FLUSH_BYTES >> 20} "
+                  "MiB read so no dirty lines remain), outside the step events",
+            "parallelism": f"replicas x{world} (no data-path collective)"}
+
+
 def flops(M, K, N):
     return 2.0 * M * N * K
 
@@ -277,8 +286,12 @@ def run_gpu(args, rank, world, local_rank):
     if rank == 0:
         quant_obj = bench_group_quant(torch, fm, synth, dev, flush)
 
-    widened = per_tensor = determ = None
+    widened = per_tensor = determ = scatter = sweep = tiny = None
     if rank == 0:
+        peaks, _ = load_peaks()
+        scatter = bench_scatter(torch, fm, synth, dev, flush)
+        sweep = bench_quant_sweep(torch, fm, synth, dev, flush, peaks["hbm_gbs"])
+        tiny = bench_tiny_config(torch, fm, synth, dev, flush)
         widened = bench_widened(torch, fm, synth, dev, flush, work[0])
         per_tensor = bench_per_tensor(torch, fm, dev, flush)
         determ = bench_deterministic(torch, fm, dev, flush)
@@ -290,7 +303,8 @@ def run_gpu(args, rank, world, local_rank):
 
     res = dict(step_ms=tot_step_ms / args.steps, gemm_ms=tot_gemm_ms / args.steps,
                quant_ms=tot_quant_ms / args.steps, wall=wall, step_flops=step_flops,
-               step_quant_bytes=step_quant_bytes, clocks=clocks, quant=quant_obj, e2e=e2e, widened=widened, per_tensor=per_tensor, determ=determ,
+               step_quant_bytes=step_quant_bytes, clocks=clocks, quant=quant_obj, e2e=e2e, widened=widened,
+               per_tensor=per_tensor, determ=determ, scatter=scatter, sweep=sweep, tiny=tiny,
                per_shape_gemm_ms=[x / args.steps for x in per_shape_gemm], launches=2 * len(work) * args.steps)
     return res
 
@@ -342,6 +356,75 @@ def bench_group_quant(torch, fm, synth, dev, flush, reps=20):
     out["masked_silu_mul_ep_decode"] = {"us": round(us, 2), "bytes": nbytes, "gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
                                         "workload": f"E={E} T={T} K={KM}, {rows} token rows"}
     return out
+
+
+def scatter_workload(torch, fm, synth, dev, M=QUANT_M, K=QUANT_K):
+    """Topk scatter of the group-128 quant: M tokens of K bf16, each quantized once and
+    written to 8 of 256 expert rows (seeded routing, expert regions padded to 128
+    rows), UE8M0 scales packed column-major.  Returns (launch, algorithmic bytes):
+    2K read and 8 x (K codes + K/512 scale words) written per token."""
+    import numpy as np
+    x = synth.quant_input(M, K, torch.bfloat16, seed=53, device=dev)
+    dst, R = synth.routing(M, topk=8, num_experts=256)
+    dst_t = torch.from_numpy(dst).to(dev)
+    q, s = fm.alloc_group_quant_outputs(R, K, 128, fm.SCALE_UE8M0_PACKED, True, device=dev)
+    written = int(np.count_nonzero(dst >= 0))
+    nbytes = M * K * 2 + written * (K + (K // 512) * 4) + dst.size * 4
+
+    def launch():
+        fm.per_token_group_quant_fp8_scatter(x, dst_t, q, s, 128, fm.SCALE_UE8M0_PACKED, True)
+    return launch, nbytes, R
+
+
+def bench_scatter(torch, fm, synth, dev, flush, reps=20):
+    launch, nbytes, R = scatter_workload(torch, fm, synth, dev)
+    us = _median_us(torch, flush, launch, reps)
+    return {"workload": f"M={QUANT_M} K={QUANT_K} bf16, group 128, topk 8 of 256 experts -> {R} rows, UE8M0 "
+                        "packed column-major scales", "us": round(us, 2), "bytes": nbytes,
+            "gbs": round(nbytes / (us * 1e-6) / 1e9, 1)}
+
+
+def bench_quant_sweep(torch, fm, synth, dev, flush, hbm_peak, reps=10):
+    """Every standalone group-quant cell of the quant configuration: tokens M in
+    1, 64, 512, 8192; hidden K in 2048, 7168; bf16 and fp16; fp32 row-major and UE8M0
+    packed column-major scales; group 128.  Cells whose ideal time at the HBM peak is
+    under 5 us are marked launch-bound (an empty launch measures a few us this way)."""
+    out = []
+    for K in (2048, 7168):
+        for M in (1, 64, 512, 8192):
+            for dt_name, dt in (("bf16", torch.bfloat16), ("fp16", torch.float16)):
+                x = synth.quant_input(M, K, dt, seed=200 + M + K, device=dev)
+                for fmt_name, fmt, cm in (("fp32_rowmajor", fm.SCALE_FP32, False),
+                                          ("ue8m0_colmajor", fm.SCALE_UE8M0_PACKED, True)):
+                    q, sc = fm.alloc_group_quant_outputs(M, K, 128, fmt, cm, device=dev)
+                    us = _median_us(torch, flush, lambda: fm.per_token_group_quant_fp8(x, q, sc, 128, fmt, cm), reps)
+                    nbytes = M * K * 3 + sc.numel() * 4
+                    ideal = nbytes / (hbm_peak * 1e9) * 1e6
+                    out.append({"M": M, "K": K, "dtype": dt_name, "scales": fmt_name, "us": round(us, 2),
+                                "gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
+                                "frac": round(nbytes / (us * 1e-6) / 1e9 / hbm_peak, 4),
+                                "bound": "launch" if ideal < 5.0 else "hbm"})
+    return out
+
+
+def bench_tiny_config(torch, fm, synth, dev, flush, reps=20):
+    """The tiny rowwise configuration: X bf16 [64, 512] group-128 quantized (fp32
+    scales), then the GEMM against a per-channel-quantized W [256, 512] with the
+    per-group A scales.  Launch-bound at this size; reported in us per launch."""
+    M, N, K = 64, 256, 512
+    X = synth.normal((M, K), 1.0, seed=synth.SEED_A, device=dev)
+    W = synth.normal((N, K), 0.02, seed=synth.SEED_B, device=dev)
+    B = torch.empty((N, K), dtype=torch.uint8, device=dev)
+    b_s = torch.empty((N, 1), dtype=torch.float32, device=dev)
+    fm.per_token_group_quant_fp8(W, B, b_s, K)
+    A = torch.empty((M, K), dtype=torch.uint8, device=dev)
+    a_s = torch.empty((M, K // 128), dtype=torch.float32, device=dev)
+    D = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    q_us = _median_us(torch, flush, lambda: fm.per_token_group_quant_fp8(X, A, a_s, 128), reps)
+    g_us = _median_us(torch, flush, lambda: fm.fp8_scaled_mm(A, B, a_s, b_s, fm.A_GROUP128 | fm.B_COL, D), reps)
+    return {"workload": "X [64,512] group-128 quant + GEMM with W [256,512], group-128 A x per-column B scales",
+            "quant_us": round(q_us, 2), "gemm_us": round(g_us, 2),
+            "gemm_tflops": round(flops(M, K, N) / (g_us * 1e-6) / 1e12, 3), "bound": "launch"}
 
 
 def _median_us(torch, flush, fn, reps):
@@ -587,6 +670,8 @@ def run_kernel_case(args):
                 fm.fp8_scaled_mm(A, B, a_s, b_s, fm.A_GROUP128_UE8M0 | fm.B_BLOCK128, D)
     elif args.kernel_case in ("quant_masked", "quant_int8", "quant_row_padded", "static_quant", "requant"):
         launch, work = _widened_case(torch, fm, synth, dev, args.kernel_case)
+    elif args.kernel_case == "scatter":
+        launch, work, _ = scatter_workload(torch, fm, synth, dev)
     else:
         fuse = args.kernel_case == "quant_fused"
         M, K = QUANT_M, QUANT_K
@@ -667,10 +752,10 @@ def run_reference(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tot_s / args.steps * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "large rowwise FP8 prefill GEMMs + per-token activation quant (sample)",
-                   "shapes_MxKxN": [list(s) for s in SHAPES], "rows_per_shape_per_step": rows},
+        "config": workload_config(world),
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-                         "sample": f"{rows} rows of each shape per step, all N"},
+                         "sample": f"{rows} rows of each of the 5 shapes per step (per-row quant + fp64 GEMM over "
+                                   "all N); the oracle times a bounded sample of the workload"},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "wall_s": round(wall, 2),
     }
@@ -691,7 +776,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--kernel-case", choices=["gemm", "gemm_block", "quant", "quant_fused", "quant_masked",
-                                              "quant_int8", "quant_row_padded", "static_quant", "requant"],
+                                              "quant_int8", "quant_row_padded", "static_quant", "requant",
+                                              "scatter"],
                     default=None,
                     help="run a single kernel on its workload (for profilers) instead of the benchmark")
     ap.add_argument("--shape", type=int, default=0, help="prefill shape index for --kernel-case gemm")
@@ -745,11 +831,7 @@ def main():
                             f"({h100_reference_tflops():.0f} TFLOP/s, sglang PR #34318 kernel table; other hardware)",
         "dtype": "e4m3 x e4m3 -> fp32 accumulate -> bf16",
         "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights, bf16, quantized on device)",
-        "config": {"workload": "large rowwise-scaled FP8 prefill GEMMs (5 shapes) + per-token activation quant",
-                   "shapes_MxKxN": [list(s) for s in SHAPES], "out": "bf16", "scales": "fp32 per-row x per-col",
-                   "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write, then {L2_FLUSH_BYTES >> 20} "
-                         "MiB read so no dirty lines remain), outside the step events",
-                   "parallelism": f"replicas x{world} (no data-path collective)"},
+        "config": workload_config(world),
         "gemm": {"tflops": round(gemm_tflops, 2), "ms_per_step": round(res["gemm_ms"], 4),
                  "per_shape_tflops": [round(flops(*s) / (t * 1e-3) / 1e12, 1)
                                       for s, t in zip(SHAPES, res["per_shape_gemm_ms"])]},
@@ -778,6 +860,17 @@ def main():
         line["group_quant"]["plain"]["traffic"] = load_traffic("group_quant", qhash)
         line["group_quant"]["fused_silu_mul"]["traffic"] = load_traffic("group_quant", qhash,
                                                                         "fused_bytes_per_launch")
+    if res["scatter"]:
+        sc = dict(res["scatter"])
+        sc["frac"] = round(sc["gbs"] / hbm_peak, 4)
+        sc["bound"] = "hbm"
+        sc["traffic"] = load_traffic("scatter", qhash)
+        line["scatter"] = sc
+    if res["sweep"]:
+        line["group_quant_sweep"] = {"note": "every standalone quant cell (group 128), event-timed, L2 flushed before "
+                                             "each launch; frac of the HBM peak", "cells": res["sweep"]}
+    if res["tiny"]:
+        line["tiny_group_gemm"] = res["tiny"]
     if res["widened"]:
         wd = res["widened"]
         for k, v in wd.items():

@@ -3,7 +3,9 @@
 // and a self-test of the bounded in-kernel wait.
 #include <cudaTypedefs.h>
 
+#include <map>
 #include <mutex>
+#include <utility>
 
 #include "common.cuh"
 #include "ptx.cuh"
@@ -18,7 +20,21 @@ std::mutex g_mu;
 int* g_status_ptr[kMaxDevices] = {};
 int g_sms[kMaxDevices] = {};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::mutex g_once_mu;   // separate from g_mu: set-ups may call num_sms() and the like
+std::map<std::pair<const void*, int>, int> g_once;
 }  // namespace
+
+int once_per_device(const void* key, const std::function<int()>& setup) {
+  int dev = 0;
+  const cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return -static_cast<int>(e);
+  std::lock_guard<std::mutex> lk(g_once_mu);
+  const auto it = g_once.find({key, dev});
+  if (it != g_once.end()) return it->second;
+  const int r = setup();
+  if (r >= 0) g_once[{key, dev}] = r;
+  return r;
+}
 
 int* status_word_device_ptr() {
   int dev = 0;

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <functional>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -21,6 +22,22 @@ int num_sms();
 //   row_stride_bytes: bytes between consecutive rows.
 bool make_tma_2d(CUtensorMap* map, void* base, CUtensorMapDataType dtype, uint64_t inner, uint64_t outer,
                  uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz);
+
+// One-time set-up per (key, current device): the first call for a pair runs
+// `setup` and stores its result if it is >= 0 (a negative result is returned and
+// not stored, so the next call tries again); later calls return the stored value.
+// Thread-safe: two host threads launching at once run the set-up once.  `setup`
+// must not call back into this function.
+int once_per_device(const void* key, const std::function<int()>& setup);
+
+// Raise `kernel`'s dynamic shared-memory limit to `bytes` once per device.
+inline cudaError_t smem_opt_in(const void* kernel, int bytes) {
+  const int r = once_per_device(kernel, [&]() {
+    const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    return e == cudaSuccess ? 0 : -static_cast<int>(e);
+  });
+  return r < 0 ? static_cast<cudaError_t>(-r) : cudaSuccess;
+}
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 

@@ -101,26 +101,16 @@ __device__ __forceinline__ void tile_coords(const GemmArgs& p, int t, int& mb, i
   nb = r / gsz;
 }
 
-__device__ __forceinline__ float a_scale_at(const GemmArgs& p, int row, int kb) {
+// Row scale of the rowwise / per-tensor A modes (the per-group modes run in
+// fp8_gemm_group_kernel); rows past M read as 0.
+__device__ __forceinline__ float a_scale_at(const GemmArgs& p, int row) {
   if (row >= p.M) return 0.0f;
-  switch (p.a_mode) {
-    case FP8MM_SCALE_A_TENSOR: return __ldg(p.a_scale);
-    case FP8MM_SCALE_A_ROW: return __ldg(p.a_scale + row);
-    case FP8MM_SCALE_A_GROUP128: return __ldg(p.a_scale + static_cast<int64_t>(row) * p.a_ld + kb);
-    case FP8MM_SCALE_A_GROUP128_COLMAJOR: return __ldg(p.a_scale + static_cast<int64_t>(kb) * p.a_ld + row);
-    default: {
-      // UE8M0 bytes packed four per int32 word, column-major: byte kb % 4 of word (kb / 4, row)
-      const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(p.a_scale) + static_cast<int64_t>(kb >> 2) * p.a_ld + row);
-      const uint32_t e = (w >> (8 * (kb & 3))) & 0xFFu;
-      return __uint_as_float(e << 23);   // 2^(e-127); e = 0 gives 0
-    }
-  }
+  return p.a_mode == FP8MM_SCALE_A_TENSOR ? __ldg(p.a_scale) : __ldg(p.a_scale + row);
 }
 
-// Block B scale of the 128-wide N block holding column n, K block kb.
-__device__ __forceinline__ float b_block_scale_at(const GemmArgs& p, int n, int kb) {
-  return __ldg(p.b_scale + static_cast<int64_t>(n >> 7) * p.b_ld + kb);
-}
+// fp32 value of a UE8M0 scale byte e: 2^(e-127), rounded to fp32 -- e = 0 is the
+// subnormal 2^-127 (bit 22 set), e = 255 overflows to +inf (the exponent field alone).
+__device__ __forceinline__ float ue8m0_to_f32(uint32_t e) { return __uint_as_float(e ? e << 23 : 0x00400000u); }
 
 // b_scale and bias for the 32 columns n0..n0+31 (zeros beyond N).
 __device__ __forceinline__ void load_col_vectors(const GemmArgs& p, int n0, float (&sb)[32], float (&bs)[32]) {
@@ -334,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t acc = acc_i & 1u;
       if (!mbar_wait(&tfull[acc], (acc_i >> 1) & 1u, abort_flag, p.status, p.timeout_ns)) break;
       tc_fence_after();
-      const float sa = a_scale_at(p, row, 0);
+      const float sa = a_scale_at(p, row);
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t r[32];
@@ -452,7 +442,7 @@ struct ScaleStream {
     return __ldg(b + kb);
   }
   __device__ __forceinline__ static float decode(uint32_t raw, int kb) {
-    if (AMODE == FP8MM_SCALE_A_GROUP128_UE8M0) return __uint_as_float(((raw >> (8 * (kb & 3))) & 0xFFu) << 23);
+    if (AMODE == FP8MM_SCALE_A_GROUP128_UE8M0) return ue8m0_to_f32((raw >> (8 * (kb & 3))) & 0xFFu);
     return __uint_as_float(raw);
   }
 };
@@ -849,7 +839,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n = n0 + t;
       vec_sb[t] = n < p.N ? (p.b_mode == 0 ? __ldg(p.b_scale) : __ldg(p.b_scale + n)) : 0.0f;
       vec_bias[t] = (p.bias && n < p.N) ? __bfloat162float(p.bias[n]) : 0.0f;
-      for (int m = t; m < BT; m += 128) vec_sa[m] = a_scale_at(p, m0 + m, 0);
+      for (int m = t; m < BT; m += 128) vec_sa[m] = a_scale_at(p, m0 + m);
     }
     // TMEM -> own shared-memory partial [BT][128] (lane = weight row within the tile)
     const int q = warp & 3;
@@ -947,14 +937,8 @@ cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorM
                    int grid, cudaStream_t st) {
   using L = Layout<BN, STAGES>;
   auto kern = fp8_gemm_kernel<BN, STAGES>;
-  static int configured_dev = -1;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (configured_dev != dev) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
-    if (e != cudaSuccess) return e;
-    configured_dev = dev;
-  }
+  const cudaError_t e = smem_opt_in(reinterpret_cast<const void*>(kern), L::ALLOC);
+  if (e != cudaSuccess) return e;
   kern<<<grid, kThreads, L::ALLOC, st>>>(ta, tb, td, p);
   return cudaGetLastError();
 }
@@ -975,20 +959,16 @@ struct GroupKernels {
   // Once per device: shared-memory opt-in for both, and whether the split kernel's
   // register count covers its setmaxnreg shares (otherwise its warps would wait).
   static cudaError_t prepare(bool* split_ok) {
-    static int dev_done = -1;
-    static bool ok = false;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev_done != dev) {
+    const int r = once_per_device(reinterpret_cast<const void*>(split), []() {
       cudaError_t e = cudaFuncSetAttribute(split, cudaFuncAttributeMaxDynamicSharedMemorySize, LS::ALLOC);
       if (e == cudaSuccess) e = cudaFuncSetAttribute(alt, cudaFuncAttributeMaxDynamicSharedMemorySize, LA::ALLOC);
       cudaFuncAttributes fa;
       if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, split);
-      if (e != cudaSuccess) return e;
-      ok = 128 * LS::REG_LO + 32 * LS::EPI_WARPS * LS::REG_HI <= LS::THREADS * fa.numRegs;
-      dev_done = dev;
-    }
-    *split_ok = ok;
+      if (e != cudaSuccess) return -static_cast<int>(e);
+      return 128 * LS::REG_LO + 32 * LS::EPI_WARPS * LS::REG_HI <= LS::THREADS * fa.numRegs ? 1 : 0;
+    });
+    if (r < 0) return static_cast<cudaError_t>(-r);
+    *split_ok = r == 1;
     return cudaSuccess;
   }
 
@@ -1034,14 +1014,8 @@ cudaError_t launch_swap(const CUtensorMap& tw, const CUtensorMap& tx, const Gemm
                         cudaStream_t st) {
   using L = SwapLayout<BT>;
   auto kern = fp8_gemm_swap_splitk_kernel<BT>;
-  static int configured_dev = -1;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (configured_dev != dev) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
-    if (e != cudaSuccess) return e;
-    configured_dev = dev;
-  }
+  const cudaError_t e = smem_opt_in(reinterpret_cast<const void*>(kern), L::ALLOC);
+  if (e != cudaSuccess) return e;
   SplitArgs sp;
   sp.splits = splits;
   sp.n_tiles = ceil_div(p.N, 128);

@@ -82,7 +82,12 @@ enum {
   FP8MM_SCALE_A_GROUP128_COLMAJOR = 0x3, /* a_scale[g*pad4(M) + m], [K/128, pad4(M)] */
   FP8MM_SCALE_A_GROUP128_UE8M0 = 0x4,  /* UE8M0 bytes packed four per int32, column-major
                                           [ceil(K/512), pad4(M)] (the group quant's output):
-                                          a_s(m, g) = 2^(byte g%4 of word (g/4, m) - 127) */
+                                          a_s(m, g) = 2^(e - 127), e = byte g%4 of word
+                                          (g/4, m), as an fp32 value: e = 0 is the subnormal
+                                          2^-127 and e = 255 is +inf (2^128 overflows fp32),
+                                          the value the quant's FP32_POW2 format gives for
+                                          the same group (finite inputs give 85 <= e <= 254,
+                                          a group holding an infinity e = 255) */
   FP8MM_SCALE_B_TENSOR = 0x00,         /* b_scale[0] */
   FP8MM_SCALE_B_COL = 0x10,            /* b_scale[n], [N] */
   FP8MM_SCALE_B_BLOCK128 = 0x20        /* b_scale[(n/128)*(K/128) + g], [ceil(N/128), K/128];
@@ -237,6 +242,7 @@ FP8MM_API int static_per_tensor_quant_fp8(const void* x, int x_dtype, const floa
  *   w, w_out        uint8 E4M3 codes [N, K], device, 16-byte aligned (w_out may be w).
  *   shard_scales    fp32 [num_shards], device.
  *   logical_widths  int64 [num_shards], HOST; rows of each shard in order, sum <= N.
+ *   max_scale_out   fp32 [1], device; must not overlap shard_scales (FP8MM_EINVAL).
  *   num_shards      1 .. 16.   K % 16 == 0.
  */
 FP8MM_API int requantize_with_max_scale_fp8(const uint8_t* w, uint8_t* w_out, const float* shard_scales,

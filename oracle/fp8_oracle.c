@@ -22,14 +22,17 @@
  *
  *  - per-token group quant (same PR, section 1 and the commit notes on the
  *    compile-time floor): per group of g consecutive elements of a row,
- *      amax = max |v| over the group's non-NaN elements (the method's
- *             absmax ignores NaN and keeps infinities),  a = max(amax, 1e-10),
+ *      amax = max |v| over the group's non-NaN elements,  a = max(amax, 1e-10),
  *      s = fl32(a / 448),  mult = fl32(448 / a)      (IEEE division),
  *      UE8M0: e = biased exponent of s (+1 if its mantissa is non-zero),
  *             s = 2^(e-127), mult = 2^(127-e)       (power of two),
  *      q = E4M3(fl32(v * mult)).
  *    The multiply is always fp32, so an fp16 input never sees the
  *    448/1e-10 multiplier overflow that the PR fixes.
+ *    NaN inputs: the PR says only that a NaN reaching the encoder's clamp
+ *    becomes +448; it does not say how the group absmax treats a NaN.  The
+ *    reading taken here leaves NaN elements out of the absmax (infinities are
+ *    kept), so a stray NaN does not poison the scale of its whole group.
  *
  *  - fused SiLU(gate)*up in front of the quant (same PR, section 2): silu(g) =
  *    g / (1 + exp(-g)) with a plain IEEE divide.  exp is the Cody-Waite
@@ -394,10 +397,14 @@ static double a_scale_at(const gemm_job* j, int64_t m, int64_t g) {
     case 2: return (double)j->a_scale[m * j->a_ld + g];
     case 3: return (double)j->a_scale[g * j->a_ld + m];
     default: {
-      /* UE8M0: byte g % 4 of word (g / 4, m); scale 2^(byte - 127) */
+      /* UE8M0: byte g % 4 of word (g / 4, m) stands for the fp32 scale
+         2^(byte - 127) (same PR, Modifications 3: the fp32 form of a UE8M0
+         scale is 2^(e-127)).  Every byte is taken by that formula and the value
+         rounded to fp32, the type the scales have everywhere else: byte 0 is the
+         subnormal 2^-127, byte 255 (2^128) overflows to +inf. */
       const uint32_t* w = (const uint32_t*)j->a_scale;
       uint32_t e = (w[(g / 4) * j->a_ld + m] >> (8 * (g % 4))) & 0xFFu;
-      return ldexp(1.0, (int)e - 127);
+      return (double)ldexpf(1.0f, (int)e - 127);
     }
   }
 }

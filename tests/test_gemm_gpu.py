@@ -4,9 +4,11 @@ Inputs: bf16 activations ~N(0,1) and weights ~N(0,0.02) quantized to E4M3 by
 the oracle (per-row / per-channel, per-tensor or group-128 scales), so no
 input of the comparison comes from the CUDA path.  Each output element must
 be within max(1 ulp, 2^-7 |ref|) of the oracle's exactly accumulated result
-(see gpu_util.check_gemm for the near-cancellation rule).  Large problems are
-compared on sampled rows that include the first and last rows and both sides
-of 128-row tile boundaries."""
+(see oracle.parity.check_gemm for the near-cancellation rule).  Large problems
+are compared on one row of every 128-row M block (at an in-block offset that
+rotates from block to block) against all N, plus the first and last rows, both
+sides of tile boundaries and random rows; one prefill shape is compared over
+its whole output."""
 import numpy as np
 import pytest
 import torch
@@ -25,8 +27,14 @@ OBMODE = {"tensor": oracle.B_TENSOR, "col": oracle.B_COL}
 
 
 def sample_rows(M, n_random=16, seed=0):
+    """Rows to compare for a large M: one in every 128-row M block, at offset
+    37 b mod 128 in block b, so that every output tile -- whatever wave, raster
+    group or tile width computed it -- has a row checked against all N; the first
+    and last two rows; both sides of block boundaries spread over M; random rows."""
     rng = np.random.default_rng(seed)
     rows = {0, 1, M - 1, M - 2}
+    for b in range((M + 127) // 128):
+        rows.add(min(M - 1, 128 * b + (37 * b) % 128))
     for b in range(128, M, 128 * max(1, M // 128 // 8)):
         rows.update({b - 1, b})
     rows.update(rng.integers(0, M, size=n_random).tolist())
@@ -81,7 +89,34 @@ def test_config2_per_tensor(M, N):
 @pytest.mark.parametrize("M,K,N", [(8320, 5376, 21504), (8320, 5376, 14336), (23216, 5376, 28672),
                                    (15760, 5376, 28672), (8320, 14336, 5376)])
 def test_config3_rowwise_large(M, K, N):
-    run_case(M, N, K, "row", "col", rows=sample_rows(M, n_random=12, seed=K), seed=M)
+    rows = sample_rows(M, n_random=12, seed=K)
+    assert len(rows) >= (M + 127) // 128
+    run_case(M, N, K, "row", "col", rows=rows, seed=M)
+
+
+def test_config3_full_output_8320x14336x5376():
+    # the prefill shape with the fewest flops (1.28 TFLOP), every one of its 44.7 M
+    # outputs against the oracle
+    stats = run_case(8320, 5376, 14336, "row", "col", seed=8320)
+    assert stats["n"] == 8320 * 5376
+
+
+def test_ue8m0_scale_bytes_at_both_ends_of_the_range():
+    # the oracle pin's case (bytes 0, 1, 127, 255) through the group-scale kernel: the
+    # kernel reads byte 0 as 2^-127 and byte 255 as +inf, as the oracle does
+    from test_oracle_gemm import ue8m0_edge_case
+    dev = require_gpu()
+    A, words, B, b_s = ue8m0_edge_case()
+    M, N = A.shape[0], B.shape[0]
+    out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    fm.fp8_scaled_mm(to_dev(A), to_dev(B), to_dev(words), to_dev(b_s), fm.A_GROUP128_UE8M0 | fm.B_COL, out)
+    torch.cuda.synchronize()
+    assert fm.get_device_status() == 0
+    ref_bits, exact, sumabs = oracle.gemm(A, B, words, b_s, oracle.A_GROUP_UE8M0, oracle.B_COL, want_exact=True)
+    got = bits(out)
+    check_gemm(got, exact, sumabs, 128, 0, "ue8m0 bytes 0/255", allow_nonfinite=True)
+    fin = np.isfinite(exact)
+    assert np.array_equal(got[fin], ref_bits[fin])      # these sums are exact: same bits
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 8, 16), (3, 24, 80), (127, 264, 144), (129, 136, 272), (200, 520, 1040),

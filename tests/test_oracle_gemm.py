@@ -167,3 +167,42 @@ def test_block_scales_and_packed_ue8m0_a_scales():
                            want_exact=True)
     _, e4, _ = oracle.gemm(A, B, a_f, np.float32(1), oracle.A_GROUP, oracle.B_TENSOR, want_exact=True)
     assert np.array_equal(e3, e4)
+
+
+def ue8m0_edge_case():
+    """Inputs of the UE8M0 byte-range pin (also run on the GPU): K = 128, every A
+    and B code 1.0 (0x38) except B row 2, all zero; so each row's single K block
+    sums to 128, or to 0 in column 2.  A scale bytes per row: 0, 1, 127, 255;
+    column scales 2^100, 2^-120, 1 and 2^100 for the other columns."""
+    M, N, K = 4, 8, 128
+    A = np.full((M, K), 0x38, np.uint8)
+    B = np.full((N, K), 0x38, np.uint8)
+    B[2] = 0
+    e = [0, 1, 127, 255]
+    words = np.zeros((1, oracle.pad4(M)), np.uint32)
+    words[0, :M] = e                      # group 0 sits in byte 0 of word 0
+    b_s = np.full(N, 2.0 ** 100, np.float32)
+    b_s[1] = 2.0 ** -120
+    b_s[2] = 1.0
+    return A, words.view(np.int32), B, b_s
+
+
+def test_ue8m0_scale_bytes_at_both_ends_of_the_range():
+    # A UE8M0 byte e stands for the fp32 scale 2^(e-127) (the Quant PR's fp32 form of
+    # a UE8M0 scale, Modifications 3), taken as an fp32 value like every other scale:
+    # byte 0 is the subnormal 2^-127 (not 0), byte 255 overflows to +inf (not the
+    # finite fp64 2^128).  Expected bf16 bits worked out by hand:
+    #   row 0, 128 * 2^-127 * 2^100 = 2^-20   -> 0x3580;  * 2^-120 = 2^-240, below
+    #          the smallest bf16 subnormal (2^-133) -> 0;  column 2: 0
+    #   row 1, 128 * 2^-126 * 2^100 = 2^-19   -> 0x3600;  2^-239 -> 0
+    #   row 2, 128 * 2^100 = 2^107            -> 0x7500;  2^-113 -> 0x0700
+    #   row 3, inf in every column with a non-zero sum (with the fp64 2^128 column 1
+    #          would be the finite 2^15); column 2: inf * 0 = NaN
+    A, words, B, b_s = ue8m0_edge_case()
+    out, exact, _ = oracle.gemm(A, B, words, b_s, oracle.A_GROUP_UE8M0, oracle.B_COL, want_exact=True)
+    assert out[0, 0] == 0x3580 and out[0, 1] == 0x0000 and out[0, 2] == 0x0000
+    assert out[1, 0] == 0x3600 and out[1, 1] == 0x0000
+    assert out[2, 0] == 0x7500 and out[2, 1] == 0x0700 and out[2, 2] == 0x0000
+    assert np.all(out[:3, 3:] == out[:3, :1])
+    assert exact[3, 0] == np.inf and exact[3, 1] == np.inf and np.isnan(exact[3, 2])
+    assert out[3, 0] == 0x7F80 and out[3, 1] == 0x7F80 and (out[3, 2] & 0x7F80) == 0x7F80 and out[3, 2] & 0x7F

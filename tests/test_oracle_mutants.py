@@ -56,6 +56,10 @@ MUTANTS = [
      [("int ex = be + ((bits & 0x7FFFFF) != 0);", "int ex = be;", 1)]),
     ("ue8m0 multiplier off by a factor two", C_SRC,
      [("mult = pow2f_exact(127 - ex);", "mult = pow2f_exact(128 - ex);", 1)]),
+    ("GEMM UE8M0 scale byte decoded in fp64 (byte 255 finite)", C_SRC,
+     [("return (double)ldexpf(1.0f, (int)e - 127);", "return ldexp(1.0, (int)e - 127);", 1)]),
+    ("GEMM UE8M0 scale byte 0 decoded as zero", C_SRC,
+     [("return (double)ldexpf(1.0f, (int)e - 127);", "return e ? (double)ldexpf(1.0f, (int)e - 127) : 0.0;", 1)]),
     # int8
     ("int8 ties away from zero", C_SRC,
      [("if (r > 0.5 || (r == 0.5 && fmod(f, 2.0) != 0.0)) n = f + 1.0;", "if (r >= 0.5) n = f + 1.0;", 1)]),
