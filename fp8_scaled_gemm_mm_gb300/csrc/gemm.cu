@@ -87,6 +87,7 @@ struct Layout {
   static constexpr int BYTES = OFF_MISC + 16;
   static constexpr int ALLOC = BYTES + 1024;  // slack to align the base to 1024
   static constexpr uint32_t TMEM_COLS = pow2_at_least(2 * BN);
+  static constexpr uint32_t ACC_STRIDE = TMEM_COLS / 2;   // accumulator 1 starts at a power-of-two column
   static_assert(B_BYTES % 1024 == 0, "B stage must keep 1024-byte alignment");
   static_assert(ALLOC <= 232448, "shared memory budget");
 };
@@ -282,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = mbar_wait(&full[stage], phase, abort_flag, p.status, p.timeout_ns);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t d = tmem_base + acc * BN;
+          const uint32_t d = tmem_base + acc * L::ACC_STRIDE;
           const uint64_t adesc = smem_desc_sw128(smem_u32(smem + L::OFF_A + stage * L::A_BYTES));
           const uint64_t bdesc = smem_desc_sw128(smem_u32(smem + L::OFF_B + stage * L::B_BYTES));
 #pragma unroll
@@ -328,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t r[32];
-        tmem_ld_32x32b_x32(lane_addr + acc * BN + c * 32, r);
+        tmem_ld_32x32b_x32(lane_addr + acc * L::ACC_STRIDE + c * 32, r);
         tmem_ld_wait();
         if (c == BN / 32 - 1) {
           tc_fence_before();
@@ -1064,13 +1065,16 @@ Config pick_config(int64_t M, int64_t N, bool deterministic, bool group_a, int s
   // lower still), so a partly idle single wave of wide tiles can beat two waves of
   // narrow ones.
   const int64_t mblk = ceil_div(M, BM);
-  const Config opts[3] = {{256, 4, false}, {128, 6, false}, {64, 8, false}};
-  const double eff[3] = {1.0, 0.6, 0.33};
+  // relative MMA rate of a 128 x N instruction stream, 3N / (512 + N): a fixed cost
+  // per K step plus one proportional to N, fitted to the measured 0.6 at N = 128
+  constexpr int kOpts = 5;
+  const Config opts[kOpts] = {{256, 4, false}, {224, 4, false}, {192, 5, false}, {128, 6, false}, {64, 8, false}};
   int best = 0;
   double best_cost = 0.0;
-  for (int i = 0; i < 3; ++i) {
+  for (int i = 0; i < kOpts; ++i) {
+    const double eff = 3.0 * opts[i].bn / (512.0 + opts[i].bn);
     const int64_t tiles = mblk * ceil_div(N, opts[i].bn);
-    const double cost = static_cast<double>((tiles + sms - 1) / sms) * opts[i].bn / eff[i];
+    const double cost = static_cast<double>((tiles + sms - 1) / sms) * opts[i].bn / eff;
     if (i == 0 || cost < best_cost) {
       best = i;
       best_cost = cost;
@@ -1194,6 +1198,10 @@ extern "C" int fp8_scaled_mm(const void* A, const void* B, const float* a_scale,
     e = group_launch(a_mode, b_mode == 2, group_split, ta, tb, td, p, grid, st);
   else if (cfg.bn == 256)
     e = launch<256, 4>(ta, tb, td, p, grid, st);
+  else if (cfg.bn == 224)
+    e = launch<224, 4>(ta, tb, td, p, grid, st);
+  else if (cfg.bn == 192)
+    e = launch<192, 5>(ta, tb, td, p, grid, st);
   else if (cfg.bn == 128)
     e = launch<128, 6>(ta, tb, td, p, grid, st);
   else

@@ -63,15 +63,24 @@ def test_prefill_shapes_take_the_widest_tile(plan):
 
 
 def test_narrow_tiles_only_when_they_save_a_wave(plan):
-    # a narrower tile is chosen only if it needs fewer waves than 256-wide tiles, or if
-    # the 256-wide tiles fit in one partly idle wave (narrower ones then use more SMs)
-    for M in (256, 384, 1024, 2048):
-        for N in (512, 1024, 1536, 2048, 4096):
+    # a narrower tile is chosen only if it needs fewer waves than 256-wide tiles, if the
+    # 256-wide tiles fit in one partly idle wave (narrower ones then use more SMs), or if
+    # in the same number of waves it leaves fewer SMs idle in the last one (M = 2048,
+    # N = 4096: 256 tiles of 256 columns are 1.68 waves, 304 tiles of 224 exactly 2)
+    for M in (256, 384, 1024, 2048, 8192):
+        for N in (512, 1024, 1536, 2048, 4096, 12288, 14336):
             (bn, _), = _configs(plan, [(M, N)])
             if bn != 256:
                 mblk = -(-M // 128)
-                waves = lambda w: -(-mblk * -(-N // w) // SMS)
-                assert waves(bn) < waves(256) or waves(256) == 1, (M, N, bn)
+                tiles = lambda w: mblk * -(-N // w)
+                waves = lambda w: -(-tiles(w) // SMS)
+                fill = lambda w: tiles(w) / (waves(w) * SMS)
+                assert waves(bn) <= waves(256), (M, N, bn)
+                assert waves(bn) < waves(256) or waves(256) == 1 or fill(bn) > fill(256), (M, N, bn)
+    (bn, _), = _configs(plan, [(2048, 4096)])
+    assert bn == 224
+    (bn, _), = _configs(plan, [(8320, 21504)])      # full waves: the widest tile
+    assert bn == 256
 
 
 def test_split_count_limits_and_maximality(plan):
