@@ -656,7 +656,7 @@ def run_kernel_case(args):
         work = flops(M, K, N)
 
         def launch():
-            fm.fp8_scaled_mm(A, B, a_s, b_s, fm.A_ROW | fm.B_COL, D)
+            fm.fp8_scaled_mm(A, B, a_s, b_s, fm.A_ROW | fm.B_COL, D, deterministic=args.deterministic)
 
         if args.kernel_case == "gemm_block":
             a_s = torch.empty(fm.scale_shape(M, K, 128, fm.SCALE_UE8M0_PACKED, True), dtype=torch.int32, device=dev)
@@ -782,6 +782,7 @@ def main():
                     help="run a single kernel on its workload (for profilers) instead of the benchmark")
     ap.add_argument("--shape", type=int, default=0, help="prefill shape index for --kernel-case gemm")
     ap.add_argument("--mnk", default=None, help="M,K,N for --kernel-case gemm instead of a prefill shape")
+    ap.add_argument("--deterministic", action="store_true", help="--kernel-case gemm in the batch-invariant mode")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

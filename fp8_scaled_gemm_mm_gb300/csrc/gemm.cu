@@ -63,9 +63,22 @@ struct GemmArgs {
   const float* b_scale;
   const __nv_bfloat16* bias;
   int out_fp16;
+  int det_splits;   // deterministic mode: K ranges summed in order (1 = no split)
   int* status;
   uint64_t timeout_ns;
 };
+
+// First K block of range r of the deterministic split (range r is [kb_begin(r), kb_begin(r + 1))).
+__host__ __device__ __forceinline__ int det_kb_begin(int r, int num_kb, int splits) {
+  return static_cast<int>(static_cast<int64_t>(r) * num_kb / splits);
+}
+
+// The deterministic mode's output value: ((acc * a_s) * b_s) + bias, each step rounded
+// once (no contraction), so that the cluster kernel and the fold kernel of that mode
+// produce the same bits from the same fp32 sum.
+__device__ __forceinline__ float det_out(float acc, float sa, float sb, float bias) {
+  return __fadd_rn(__fmul_rn(__fmul_rn(acc, sa), sb), bias);
+}
 
 __host__ __device__ constexpr uint32_t pow2_at_least(uint32_t v) {
   uint32_t r = 32;
@@ -382,6 +395,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 // f32x2 form needs register pairs the TMEM loads do not produce, and the moves cost
 // more than the packing saves.
 
+// AMODE of fp8_gemm_group_kernel for the deterministic split: every K range of the
+// split goes to its own accumulator and is folded by plain fp32 adds in range order;
+// the A scale (per tensor or per row) comes after the sum, as in the epilogue.
+constexpr int kAModeDetFold = 15;
+
 template <int BN, int STAGES, int NACC, int SPLIT, bool RS>
 struct GroupLayout {
   static constexpr int EPI_WARPS = 4 * SPLIT;
@@ -464,6 +482,7 @@ __global__ void __launch_bounds__(GroupLayout<BN, STAGES, NACC, SPLIT, RS>::THRE
                           const __grid_constant__ CUtensorMap tmD, const GemmArgs p) {
   using L = GroupLayout<BN, STAGES, NACC, SPLIT, RS>;
   constexpr int HALF = L::WCOLS;
+  constexpr bool DET = AMODE == kAModeDetFold;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
@@ -541,7 +560,44 @@ __global__ void __launch_bounds__(GroupLayout<BN, STAGES, NACC, SPLIT, RS>::THRE
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue
-    if (lane == 0) {
+    if (lane == 0 && DET) {
+      // deterministic fold: each K range of the split accumulates into its own buffer
+      constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
+      uint32_t stage = 0, phase = 0, acc_i = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < p.tiles; t += gridDim.x) {
+        for (int r = 0; ok && r < p.det_splits; ++r) {
+          const int b0 = det_kb_begin(r, p.num_kb, p.det_splits), b1 = det_kb_begin(r + 1, p.num_kb, p.det_splits);
+          const uint32_t acc = acc_i % NACC;
+          ok = mbar_wait(&tempty[acc], ((acc_i / NACC) & 1u) ^ 1u, abort_flag, p.status, p.timeout_ns);
+          if (!ok) break;
+          tc_fence_after();
+          for (int kb = b0; kb < b1; ++kb) {
+            ok = mbar_wait(&full[stage], phase, abort_flag, p.status, p.timeout_ns);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t d = tmem_base + acc * BN;
+            const uint64_t adesc = smem_desc_sw128(smem_u32(smem + L::OFF_A + stage * L::A_BYTES));
+            const uint64_t bdesc = smem_desc_sw128(smem_u32(smem + L::OFF_B + stage * L::B_BYTES));
+#pragma unroll
+            for (int k = 0; k < BK / UMMA_K; ++k)
+              mma_f8f6f4(d, adesc + static_cast<uint64_t>(k * UMMA_K / 16),
+                         bdesc + static_cast<uint64_t>(k * UMMA_K / 16), idesc, (kb > b0 || k != 0) ? 1u : 0u);
+            mma_commit(&empty[stage]);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (!ok) break;
+          mma_commit(&tfull[acc]);
+          ++acc_i;
+        }
+      }
+      mma_commit(drain);
+      volatile int never = 0;
+      mbar_wait(drain, 0, &never, p.status, p.timeout_ns);
+    } else if (lane == 0) {
       constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
       uint32_t stage = 0, phase = 0, acc_i = 0;
       bool ok = true;
@@ -586,7 +642,67 @@ __global__ void __launch_bounds__(GroupLayout<BN, STAGES, NACC, SPLIT, RS>::THRE
     uint32_t acc_i = 0;
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + h * HALF;
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < p.tiles; t += gridDim.x) {
+    for (int t = blockIdx.x; DET && ok && t < p.tiles; t += gridDim.x) {
+      // deterministic fold: acc = p_0, then acc += p_r in range order, then the
+      // row scale, column scale and bias by det_out
+      int mb, nb;
+      tile_coords(p, t, mb, nb);
+      const int row = mb * BM + q * 32 + lane;
+      const int r0 = mb * BM + q * 32;
+      const int nbase = nb * BN;
+      float accum[HALF];
+      for (int r = 0; ok && r < p.det_splits; ++r) {
+        const uint32_t acc = acc_i % NACC;
+        ok = mbar_wait(&tfull[acc], (acc_i / NACC) & 1u, abort_flag, p.status, p.timeout_ns);
+        if (!ok) break;
+        tc_fence_after();
+        // two 32-column loads in flight: chunk c + 1 is requested before chunk c is added
+        uint32_t rv[2][32];
+        tmem_ld_32x32b_x32(lane_addr + acc * BN, rv[0]);
+#pragma unroll
+        for (int c = 0; c < HALF / 32; ++c) {
+          tmem_ld_wait();
+          if (c + 1 < HALF / 32) tmem_ld_32x32b_x32(lane_addr + acc * BN + (c + 1) * 32, rv[(c + 1) & 1]);
+          if (c + 1 == HALF / 32) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[acc]);
+          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            accum[c * 32 + j] =
+                r == 0 ? __uint_as_float(rv[c & 1][j]) : __fadd_rn(accum[c * 32 + j], __uint_as_float(rv[c & 1][j]));
+        }
+        ++acc_i;
+      }
+      if (!ok) break;
+      const float sa = a_scale_at(p, row);
+      const float sb_t = p.b_mode == 0 ? __ldg(p.b_scale) : 1.0f;
+#pragma unroll
+      for (int c = 0; c < HALF / 32; ++c) {
+        const int n0 = nbase + h * HALF + c * 32;
+        uint32_t w[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int n = n0 + 2 * j;   // N is a multiple of 8, so n < N covers n + 1
+          float s0 = sb_t, s1 = sb_t, b0 = 0.0f, b1 = 0.0f;
+          if (n < p.N) {
+            if (p.b_mode == 1) {
+              s0 = __ldg(p.b_scale + n);
+              s1 = __ldg(p.b_scale + n + 1);
+            }
+            if (p.bias) {
+              b0 = __bfloat162float(p.bias[n]);
+              b1 = __bfloat162float(p.bias[n + 1]);
+            }
+          }
+          w[j] = pack2(det_out(accum[c * 32 + 2 * j], sa, s0, b0), det_out(accum[c * 32 + 2 * j + 1], sa, s1, b1),
+                       p.out_fp16);
+        }
+        if (store_block(&tmD, stage_buf + dbuf * L::D_BYTES, w, lane, n0, r0, p.M, p.N)) dbuf ^= 1;
+      }
+    }
+    for (int t = blockIdx.x; !DET && ok && t < p.tiles; t += gridDim.x) {
       int mb, nb;
       tile_coords(p, t, mb, nb);
       const int row = mb * BM + q * 32 + lane;
@@ -926,6 +1042,216 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ------------------------------------- deterministic split, small M: cluster
+//
+// The batch-invariant mode splits K into S ranges fixed by N and K (never by M).  For
+// few rows the S CTAs of a cluster each accumulate one range of a 128 x BN tile in
+// TMEM (the same instruction shape and K order as the fold kernel), copy the valid
+// rows of their fp32 partial into shared memory (over the drained ring), and after a
+// cluster barrier CTA r sums its share of the tile's outputs over the S partials in
+// range order through distributed shared memory -- ((p_0 + p_1) + p_2) ... exactly as
+// the fold kernel adds its range accumulators -- and applies det_out.
+
+template <int BN, int STAGES>
+struct DetLayout {
+  static constexpr int A_BYTES = BM * BK;
+  static constexpr int B_BYTES = BN * BK;
+  static constexpr int RING = STAGES * (A_BYTES + B_BYTES);
+  static constexpr int PSTRIDE = BN + 4;             // floats per partial row (conflict-free v4 stores)
+  static constexpr int PART = BM * PSTRIDE * 4;
+  static constexpr int DATA = RING > PART ? RING : PART;
+  static constexpr int OFF_BAR = DATA;
+  static constexpr int NBARS = 2 * STAGES + 2;
+  static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
+  static constexpr int ALLOC = OFF_MISC + 16 + 1024;
+  static constexpr uint32_t TMEM_COLS = pow2_at_least(BN);
+  static_assert((A_BYTES + B_BYTES) % 1024 == 0, "stages must keep 1024-byte alignment");
+  static_assert(ALLOC <= 232448, "shared memory budget");
+};
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+    fp8_gemm_det_cluster_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                                const GemmArgs p, void* out) {
+  using L = DetLayout<BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* drain = tfull + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int S = p.det_splits;
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int n0 = (blockIdx.x / S) * BN;
+  const int m0 = blockIdx.y * BM;
+  const int rows = min(BM, p.M - m0);                 // valid rows of this tile
+  const int kb0 = det_kb_begin(rank, p.num_kb, S), kb1 = det_kb_begin(rank + 1, p.num_kb, S);
+  constexpr int STAGE_BYTES = L::A_BYTES + L::B_BYTES;
+
+  // the first ring's worth of loads goes out as soon as the barriers exist
+  const int pre = kb1 - kb0 < STAGES ? kb1 - kb0 : STAGES;
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(tfull, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    for (int j = 0; j < pre; ++j) {
+      mbar_arrive_expect_tx(&full[j], STAGE_BYTES);
+      uint8_t* st = smem + j * STAGE_BYTES;
+      tma_load_2d(&tmA, &full[j], st, (kb0 + j) * BK, m0);
+      tma_load_2d(&tmB, &full[j], st + L::A_BYTES, (kb0 + j) * BK, n0);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, L::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  float* part = reinterpret_cast<float*>(smem);       // [rows][PSTRIDE], valid after the mainloop
+
+  if (warp == 0) {
+    if (lane == 0) {
+      uint32_t stage = pre % STAGES, phase = pre == STAGES ? 1u : 0u;
+      int issued = pre;
+      for (int kb = kb0 + pre; kb < kb1; ++kb) {
+        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status, p.timeout_ns)) break;
+        mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+        uint8_t* st = smem + stage * STAGE_BYTES;
+        tma_load_2d(&tmA, &full[stage], st, kb * BK, m0);
+        tma_load_2d(&tmB, &full[stage], st + L::A_BYTES, kb * BK, n0);
+        ++issued;
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      const int outstanding = issued < STAGES ? issued : STAGES;
+      for (int j = 1; j <= outstanding; ++j) {
+        int s = static_cast<int>(stage) - j;
+        uint32_t ph = phase;
+        if (s < 0) {
+          s += STAGES;
+          ph ^= 1u;
+        }
+        volatile int never = 0;
+        mbar_wait(&full[s], ph, &never, p.status, p.timeout_ns);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
+      uint32_t stage = 0, phase = 0;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!mbar_wait(&full[stage], phase, abort_flag, p.status, p.timeout_ns)) break;
+        tc_fence_after();
+        uint8_t* st = smem + stage * STAGE_BYTES;
+        const uint64_t adesc = smem_desc_sw128(smem_u32(st));
+        const uint64_t bdesc = smem_desc_sw128(smem_u32(st + L::A_BYTES));
+#pragma unroll
+        for (int k = 0; k < BK / UMMA_K; ++k)
+          mma_f8f6f4(tmem_base, adesc + static_cast<uint64_t>(k * UMMA_K / 16),
+                     bdesc + static_cast<uint64_t>(k * UMMA_K / 16), idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+        mma_commit(&empty[stage]);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      mma_commit(tfull);
+      mma_commit(drain);
+      volatile int never = 0;
+      mbar_wait(drain, 0, &never, p.status, p.timeout_ns);
+    }
+  } else {
+    // TMEM -> own partial: lane = row within the tile; the valid rows only
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    if (q * 32 < rows && mbar_wait(tfull, 0, abort_flag, p.status, p.timeout_ns)) {
+      tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + c * 32, r);
+        tmem_ld_wait();
+        if (row < rows) {
+          float4* dst = reinterpret_cast<float4*>(part + row * L::PSTRIDE + c * 32);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            dst[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                 __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+        }
+      }
+    }
+    tc_fence_before();
+  }
+
+  __syncwarp();
+  cluster_sync_all();   // every partial of the cluster is in shared memory, every abort flag final
+
+  // a CTA that gave up left stale data in its partial: then no CTA of the cluster
+  // writes the tile (the status word already holds the error)
+  bool any_abort = false;
+  for (int s2 = 0; s2 < S; ++s2)
+    any_abort |= ld_dsmem_u32(mapa_shared(smem_u32(const_cast<int*>(abort_flag)), static_cast<uint32_t>(s2))) != 0;
+
+  if (!any_abort) {
+    // CTA rank takes outputs [i0, i1) of the tile's rows x BN/4 column quads
+    constexpr int QUADS = BN / 4;
+    const int items = rows * QUADS;
+    const int i0 = static_cast<int>(static_cast<int64_t>(rank) * items / S);
+    const int i1 = static_cast<int>(static_cast<int64_t>(rank + 1) * items / S);
+    const uint32_t part_addr = smem_u32(part);
+    for (int i = i0 + static_cast<int>(threadIdx.x); i < i1; i += kThreads) {
+      const int row = i / QUADS;
+      const int col = (i - row * QUADS) * 4;
+      const int n = n0 + col;
+      if (n >= p.N) continue;     // N is a multiple of 8: a quad is wholly in or out
+      const uint32_t off = static_cast<uint32_t>((row * L::PSTRIDE + col) * 4);
+      float4 acc = ld_dsmem_f32x4(mapa_shared(part_addr + off, 0));
+      for (int s2 = 1; s2 < S; ++s2) {
+        const float4 v = ld_dsmem_f32x4(mapa_shared(part_addr + off, static_cast<uint32_t>(s2)));
+        acc.x = __fadd_rn(acc.x, v.x);
+        acc.y = __fadd_rn(acc.y, v.y);
+        acc.z = __fadd_rn(acc.z, v.z);
+        acc.w = __fadd_rn(acc.w, v.w);
+      }
+      const float sa = a_scale_at(p, m0 + row);
+      float sb[4], bs[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        sb[j] = p.b_mode == 0 ? __ldg(p.b_scale) : __ldg(p.b_scale + n + j);
+        bs[j] = p.bias ? __bfloat162float(p.bias[n + j]) : 0.0f;
+      }
+      const uint32_t lo = pack2(det_out(acc.x, sa, sb[0], bs[0]), det_out(acc.y, sa, sb[1], bs[1]), p.out_fp16);
+      const uint32_t hi = pack2(det_out(acc.z, sa, sb[2], bs[2]), det_out(acc.w, sa, sb[3], bs[3]), p.out_fp16);
+      *reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + static_cast<int64_t>(m0 + row) * p.N + n) =
+          make_uint2(lo, hi);
+    }
+  }
+
+  __syncwarp();
+  cluster_sync_all();   // no CTA leaves while others may still read its partial
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, L::TMEM_COLS);
+  }
+}
+
 // ---------------------------------------------------------------- host side
 
 struct Config {
@@ -1050,6 +1376,92 @@ int pick_splits(int64_t M, int64_t N, int num_kb, int sms) {
   return s;
 }
 
+// ----------------------------------------------- deterministic split: host side
+
+// Tile width of the deterministic mode, from N alone.
+int det_bn(int64_t N) { return N >= 1024 ? 256 : (N >= 256 ? 128 : 64); }
+
+// K ranges of the deterministic mode, from N and K alone: enough ranges that a small-M
+// problem spreads its weight stream over about kDetTargetCtas CTAs, at most eight
+// (the cluster size) and at least two K blocks each.  A fixed target, not the
+// device's SM count: the split must not depend on anything but N and K.  The target
+// trades the two ends: every range adds a fold to each tile of a large problem
+// (about 2 % of its time each at K = 4096), while too few leave a small problem's
+// weight stream on too few SMs; measured on K = 4096, N = 4096, a target of 64
+// (four ranges) costs 1.02-1.17x the normal launch at M <= 16 and 1.2x at M = 4096,
+// 152 (eight ranges, clusters of eight 197 KB CTAs) 1.5x and 1.45x.
+constexpr int kDetTargetCtas = 64;
+int det_splits(int64_t N, int num_kb) {
+  const int64_t n_tiles = (N + det_bn(N) - 1) / det_bn(N);
+  int64_t s = kDetTargetCtas / n_tiles;
+  s = s < 8 ? s : 8;
+  s = s < num_kb / 2 ? s : num_kb / 2;
+  return s < 1 ? 1 : static_cast<int>(s);
+}
+
+template <int BN, int STAGES>
+cudaError_t launch_det_cluster(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& p, void* out,
+                               cudaStream_t st) {
+  using L = DetLayout<BN, STAGES>;
+  auto kern = fp8_gemm_det_cluster_kernel<BN, STAGES>;
+  const cudaError_t e = smem_opt_in(reinterpret_cast<const void*>(kern), L::ALLOC);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.n_blocks * p.det_splits), static_cast<unsigned>(p.m_blocks), 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = L::ALLOC;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(p.det_splits);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, ta, tb, p, out);
+}
+
+// The fold form of the deterministic split for each tile width: 128 x 256 with the
+// register split of the group kernel (eight epilogue warps), 128 x 128 and 128 x 64
+// with four.
+template <int BN> struct DetFold;
+template <> struct DetFold<256> {
+  using L = GroupLayout<256, 4, 2, 2, true>;
+  static constexpr auto kern = fp8_gemm_group_kernel<256, 4, 2, 2, true, kAModeDetFold, false>;
+};
+template <> struct DetFold<128> {
+  using L = GroupLayout<128, 6, 2, 1, false>;
+  static constexpr auto kern = fp8_gemm_group_kernel<128, 6, 2, 1, false, kAModeDetFold, false>;
+};
+template <> struct DetFold<64> {
+  using L = GroupLayout<64, 8, 2, 1, false>;
+  static constexpr auto kern = fp8_gemm_group_kernel<64, 8, 2, 1, false, kAModeDetFold, false>;
+};
+
+// Once per device: shared-memory opt-in, and whether the fold kernel may run (with a
+// register split, only if the compiled register count covers its shares).  Returns 1
+// if it may, 0 if not, or a negative CUDA error.
+template <int BN>
+int det_fold_prepare() {
+  using F = DetFold<BN>;
+  return once_per_device(reinterpret_cast<const void*>(F::kern), []() {
+    cudaError_t e = cudaFuncSetAttribute(F::kern, cudaFuncAttributeMaxDynamicSharedMemorySize, F::L::ALLOC);
+    cudaFuncAttributes fa;
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, F::kern);
+    if (e != cudaSuccess) return -static_cast<int>(e);
+    if (!F::L::FIRST_EPI || F::L::FIRST_EPI == 2) return 1;   // no register split
+    return 128 * F::L::REG_LO + 32 * F::L::EPI_WARPS * F::L::REG_HI <= F::L::THREADS * fa.numRegs ? 1 : 0;
+  });
+}
+
+template <int BN>
+cudaError_t launch_det_fold(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td, const GemmArgs& p,
+                            int grid, cudaStream_t st) {
+  using F = DetFold<BN>;
+  F::kern<<<grid, F::L::THREADS, F::L::ALLOC, st>>>(ta, tb, td, p);
+  return cudaGetLastError();
+}
+
 // Shape-keyed tile table.  Deterministic mode picks its tile from N alone, so every M
 // (and every prefix / suffix of the rows) runs the same tile, K order and instruction;
 // otherwise the width with the smallest estimated time wins.
@@ -1136,10 +1548,52 @@ extern "C" int fp8_scaled_mm(const void* A, const void* B, const float* a_scale,
   p.b_scale = b_scale;
   p.bias = static_cast<const __nv_bfloat16*>(bias);
   p.out_fp16 = out_dtype == FP8MM_DTYPE_FP16;
+  p.det_splits = 1;
   p.status = status;
   p.timeout_ns = kWaitTimeoutNs;
 
-  if (!deterministic && !group_a && M <= 128) {
+  if (deterministic && !group_a) {
+    // batch-invariant split: the tile width from N, the K ranges from N and K; the
+    // cluster kernel when the whole problem fits in one wave of clusters, else the
+    // persistent fold kernel -- the same bits either way
+    const int bn = det_bn(N);
+    p.det_splits = det_splits(N, p.num_kb);
+    p.m_blocks = ceil_div(M, BM);
+    p.n_blocks = ceil_div(N, bn);
+    p.tiles = p.m_blocks * p.n_blocks;
+    const int fold_ok = bn == 256 ? det_fold_prepare<256>() : (bn == 128 ? det_fold_prepare<128>() : det_fold_prepare<64>());
+    if (fold_ok < 0) return FP8MM_ECUDA;
+    CUtensorMap ta, tb, td;
+    if (!make_tma_2d(&ta, const_cast<void*>(A), CU_TENSOR_MAP_DATA_TYPE_UINT8, K, M, lda, BK, BM,
+                     CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tma_2d(&tb, const_cast<void*>(B), CU_TENSOR_MAP_DATA_TYPE_UINT8, K, N, ldb, BK, bn,
+                     CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tma_2d(&td, out, out_dtype == FP8MM_DTYPE_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                             : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                     N, M, N * 2, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+      return FP8MM_ECUDA;
+    cudaError_t e;
+    if (fold_ok == 0 || static_cast<int64_t>(p.tiles) * p.det_splits <= sms) {
+      if (bn == 256)
+        e = launch_det_cluster<256, 4>(ta, tb, p, out, st);
+      else if (bn == 128)
+        e = launch_det_cluster<128, 6>(ta, tb, p, out, st);
+      else
+        e = launch_det_cluster<64, 8>(ta, tb, p, out, st);
+    } else {
+      p.raster = 8;
+      const int grid = p.tiles < sms ? p.tiles : sms;
+      if (bn == 256)
+        e = launch_det_fold<256>(ta, tb, td, p, grid, st);
+      else if (bn == 128)
+        e = launch_det_fold<128>(ta, tb, td, p, grid, st);
+      else
+        e = launch_det_fold<64>(ta, tb, td, p, grid, st);
+    }
+    return e == cudaSuccess ? FP8MM_OK : FP8MM_ECUDA;
+  }
+
+  if (!group_a && M <= 128) {
     // small M: swap-AB with split-K over a cluster
     const int bt = M <= 16 ? 16 : (M <= 32 ? 32 : (M <= 64 ? 64 : 128));
     const int splits = pick_splits(M, N, p.num_kb, sms);

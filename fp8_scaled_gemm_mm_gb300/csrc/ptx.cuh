@@ -250,6 +250,12 @@ __device__ __forceinline__ float4 ld_dsmem_f32x4(uint32_t addr) {
   return v;
 }
 
+__device__ __forceinline__ uint32_t ld_dsmem_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
 // All threads of all CTAs of the cluster; orders shared-memory writes before it
 // with distributed shared-memory reads after it.
 __device__ __forceinline__ void cluster_sync_all() {

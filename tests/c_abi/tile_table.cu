@@ -3,6 +3,7 @@
 // queries read from stdin, one per line:
 //   config M N deterministic group_a sms   ->  "bn stages"
 //   splits M N num_kb sms                  ->  "S"
+//   det N num_kb                           ->  "bn S" (deterministic tile width, K ranges)
 // Built and run by tests/test_tile_table.py.
 #include "../../fp8_scaled_gemm_mm_gb300/csrc/api.cu"
 #include "../../fp8_scaled_gemm_mm_gb300/csrc/gemm.cu"
@@ -24,6 +25,11 @@ int main() {
       int num_kb, sms;
       if (std::scanf("%lld %lld %d %d", &M, &N, &num_kb, &sms) != 4) return 2;
       std::printf("%d\n", fp8mm::pick_splits(M, N, num_kb, sms));
+    } else if (std::strcmp(op, "det") == 0) {
+      long long N;
+      int num_kb;
+      if (std::scanf("%lld %d", &N, &num_kb) != 2) return 2;
+      std::printf("%d %d\n", fp8mm::det_bn(N), fp8mm::det_splits(N, num_kb));
     } else {
       return 2;
     }

@@ -98,3 +98,22 @@ def test_split_count_limits_and_maximality(plan):
         if s > 1:
             assert limits_ok(M, N, kb, s), (M, N, kb, s)
         assert not limits_ok(M, N, kb, s + 1), (M, N, kb, s)   # the largest count that keeps them
+
+
+def test_deterministic_split_depends_on_n_and_k_only(plan):
+    # the batch-invariant K split: the tile width from N alone (the same as the table's
+    # deterministic row), at most eight K ranges (one cluster) of at least two K blocks,
+    # and one range when K is a single block (the K = 80 tail case)
+    Ns = (8, 64, 256, 1000, 1024, 4096, 12288, 14336, 28672)
+    kbs = (1, 2, 3, 5, 32, 42, 112)
+    got = plan([f"det {N} {kb}" for N in Ns for kb in kbs])
+    cfg = {N: c for N, c in zip(Ns, _configs(plan, [(1, N) for N in Ns], det=1))}
+    for (N, kb), (bn, s) in zip([(N, kb) for N in Ns for kb in kbs], got):
+        assert bn == cfg[N][0], (N, bn)
+        assert 1 <= s <= 8, (N, kb, s)
+        assert s == 1 or kb // s >= 2, (N, kb, s)
+        if kb == 1:
+            assert s == 1
+    # the workloads' shapes: K = 4096 (32 blocks): four ranges for N = 4096, eight for N = 64
+    assert plan(["det 4096 32"]) == [(256, 4)]
+    assert plan(["det 64 32"]) == [(64, 8)]
