@@ -201,3 +201,32 @@ def test_block_scaled_gemm(ue8m0_a):
     _block_case(512, 7168, 2048, 11, ue8m0_a, rows=sample_rows(512, seed=1))
     _block_case(300, 1000, 1024, 12, ue8m0_a)
     _block_case(1, 136, 256, 13, ue8m0_a)
+
+
+@pytest.mark.parametrize("M,N,K,a_mode,b_mode,out_dtype,bias", [
+    (2048, 4096, 4096, "tensor", "tensor", 0, False),   # the per-tensor configuration's tail-wave shape
+    (4096, 4096, 4096, "row", "col", 0, False),
+    (1937, 12280, 4096, "row", "col", 1, True),          # ragged M and N, fp16 out, bias
+])
+def test_tail_wave_shapes(M, N, K, a_mode, b_mode, out_dtype, bias):
+    # shapes whose 256-wide tiles leave the last wave badly filled (the tile table then
+    # prefers 224- or 192-wide tiles): every output against the oracle, and a second
+    # call bit-identical to the first
+    dev = require_gpu()
+    A, a_s, B, b_s = gemm_inputs(M, N, K, a_mode, b_mode, seed_a=M, seed_b=N)
+    bias_bits = synth.to_bits(synth.normal((N,), 0.1, seed=synth.SEED_BIAS)) if bias else None
+    odt = torch.bfloat16 if out_dtype == 0 else torch.float16
+    args = (to_dev(A), to_dev(B), to_dev(np.ascontiguousarray(a_s, np.float32)),
+            to_dev(np.ascontiguousarray(b_s, np.float32)), AMODE[a_mode] | BMODE[b_mode])
+    biast = to_dev(bias_bits).view(torch.bfloat16) if bias else None
+    outs = []
+    for _ in range(2):
+        out = torch.empty((M, N), dtype=odt, device=dev)
+        fm.fp8_scaled_mm(*args, out, bias=biast)
+        outs.append(out)
+    torch.cuda.synchronize()
+    assert fm.get_device_status() == 0
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    _, exact, sumabs = oracle.gemm(A, B, a_s, b_s, OAMODE[a_mode], OBMODE[b_mode], bias_bits=bias_bits,
+                                   out_dtype=out_dtype, want_exact=True)
+    check_gemm(bits(outs[0]), exact, sumabs, K, out_dtype, f"tail wave M{M} N{N} K{K}")

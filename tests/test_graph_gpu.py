@@ -26,6 +26,7 @@ def _pipeline(bufs):
     fm.per_token_group_quant_fp8(b["x"], b["ag"], b["ag_s"], 128, fm.SCALE_UE8M0_PACKED, True)
     fm.fp8_scaled_mm(b["ag"], b["w"], b["ag_s"], b["w_blk"], fm.A_GROUP128_UE8M0 | fm.B_BLOCK128, b["outg"])
     fm.silu_and_mul_masked_post_quant_fp8(b["xm"], b["mm"], b["qm"], b["sm"], 128)
+    fm.fp8_scaled_mm(b["sa"], b["sw"], b["ss"], b["ss"], fm.A_TENSOR | fm.B_TENSOR, b["outsk"])   # a tail-wave shape
 
 
 def _make(dev):
@@ -53,6 +54,12 @@ def _make(dev):
         outd=torch.empty((Md, N), dtype=torch.bfloat16, device=dev),
         outdet=torch.empty((Md, N), dtype=torch.bfloat16, device=dev),
         outg=torch.empty((M, N), dtype=torch.bfloat16, device=dev),
+        sa=torch.randint(0, 126, (2048, 4096), generator=torch.Generator(device=dev).manual_seed(5),
+                         dtype=torch.uint8, device=dev),
+        sw=torch.randint(0, 126, (4096, 4096), generator=torch.Generator(device=dev).manual_seed(6),
+                         dtype=torch.uint8, device=dev),
+        ss=torch.full((1,), 0.01, dtype=torch.float32, device=dev),
+        outsk=torch.empty((2048, 4096), dtype=torch.bfloat16, device=dev),
         qm=torch.zeros((E, T, KM), dtype=torch.uint8, device=dev),
         sm=torch.zeros(fm.masked_scale_shape(E, T, KM, 128, fm.SCALE_UE8M0_PACKED, True), dtype=torch.int32,
                        device=dev),
@@ -67,7 +74,7 @@ def _fill(b, seed, dev):
                                     device=dev).reshape(b["xm"].shape))
 
 
-OUTS = ("a", "a_s", "out", "ad", "outd", "outdet", "ag", "ag_s", "outg", "qm", "sm")
+OUTS = ("a", "a_s", "out", "ad", "outd", "outdet", "ag", "ag_s", "outg", "qm", "sm", "outsk")
 
 
 def test_graph_replay_matches_eager():
