@@ -286,7 +286,7 @@ def run_gpu(args, rank, world, local_rank):
     if rank == 0:
         quant_obj = bench_group_quant(torch, fm, synth, dev, flush)
 
-    widened = per_tensor = determ = scatter = sweep = tiny = None
+    widened = per_tensor = determ = scatter = sweep = tiny = decode = None
     if rank == 0:
         peaks, _ = load_peaks()
         scatter = bench_scatter(torch, fm, synth, dev, flush)
@@ -295,6 +295,7 @@ def run_gpu(args, rank, world, local_rank):
         widened = bench_widened(torch, fm, synth, dev, flush, work[0])
         per_tensor = bench_per_tensor(torch, fm, dev, flush)
         determ = bench_deterministic(torch, fm, dev, flush)
+        decode = bench_decode_step(torch, fm, synth, dev, flush, peaks["hbm_gbs"])
 
     # ---- end to end through the C ABI with host buffers
     e2e = None
@@ -304,7 +305,7 @@ def run_gpu(args, rank, world, local_rank):
     res = dict(step_ms=tot_step_ms / args.steps, gemm_ms=tot_gemm_ms / args.steps,
                quant_ms=tot_quant_ms / args.steps, wall=wall, step_flops=step_flops,
                step_quant_bytes=step_quant_bytes, clocks=clocks, quant=quant_obj, e2e=e2e, widened=widened,
-               per_tensor=per_tensor, determ=determ, scatter=scatter, sweep=sweep, tiny=tiny,
+               per_tensor=per_tensor, determ=determ, scatter=scatter, sweep=sweep, tiny=tiny, decode=decode,
                per_shape_gemm_ms=[x / args.steps for x in per_shape_gemm], launches=2 * len(work) * args.steps)
     return res
 
@@ -532,6 +533,44 @@ def bench_per_tensor(torch, fm, dev, flush, reps=10):
                         "gbs": round(nbytes / (us * 1e-6) / 1e9, 1), "bound": "hbm" if M <= 128 else "tensor"})
             del A, D
         del B
+    return out
+
+
+def bench_decode_step(torch, fm, synth, dev, flush, hbm_peak, reps=10):
+    """Decode-shaped linear, K = 4096: the per-token quant of x [M, K] bf16 (one fp32
+    scale per row) followed by the rowwise GEMM against a per-channel E4M3 weight
+    [N, K], timed as one pair (the GEMM is launched as a programmatic dependent of the
+    quant, so its set-up and first weight prefetches overlap the quant's end), next to
+    each kernel alone.  Bytes: x read, codes and scales written and read back, the
+    weight and the bf16 output."""
+    K = 4096
+    out = []
+    for N in (4096, 14336):
+        W = synth.normal((N, K), 0.02, seed=41, device=dev)
+        B = torch.empty((N, K), dtype=torch.uint8, device=dev)
+        b_s = torch.empty((N, 1), dtype=torch.float32, device=dev)
+        fm.per_token_group_quant_fp8(W, B, b_s, K)
+        del W
+        for M in (1, 16, 64):
+            x = synth.normal((M, K), 1.0, seed=42 + M, device=dev)
+            A = torch.empty((M, K), dtype=torch.uint8, device=dev)
+            a_s = torch.empty((M, 1), dtype=torch.float32, device=dev)
+            D = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            quant = lambda: fm.per_token_group_quant_fp8(x, A, a_s, K)
+            gemm = lambda: fm.fp8_scaled_mm(A, B, a_s, b_s, fm.A_ROW | fm.B_COL, D)
+
+            def pair():
+                quant()
+                gemm()
+            t_pair = _median_us(torch, flush, pair, reps)
+            t_q = _median_us(torch, flush, quant, reps)
+            t_g = _median_us(torch, flush, gemm, reps)
+            nbytes = 2 * M * K + 2 * (M * K + 4 * M) + N * K + 4 * N + 2 * M * N
+            out.append({"M": M, "N": N, "K": K, "us_pair": round(t_pair, 2), "us_quant_alone": round(t_q, 2),
+                        "us_gemm_alone": round(t_g, 2), "gbs": round(nbytes / (t_pair * 1e-6) / 1e9, 1),
+                        "frac": round(nbytes / (t_pair * 1e-6) / 1e9 / hbm_peak, 4)})
+            del x, A, a_s, D
+        del B, b_s
     return out
 
 
@@ -889,6 +928,11 @@ def main():
                                              "each launch; frac of the HBM peak", "cells": res["sweep"]}
     if res["tiny"]:
         line["tiny_group_gemm"] = res["tiny"]
+    if res["decode"]:
+        line["decode_step_k4096"] = {"note": "per-token quant + rowwise GEMM timed as one pair (the GEMM a "
+                                             "programmatic dependent of the quant) and each alone; L2 flushed "
+                                             "before each; frac of the HBM peak for the pair's bytes",
+                                     "shapes": res["decode"]}
     if res["widened"]:
         wd = res["widened"]
         for k, v in wd.items():

@@ -245,6 +245,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // A and its scales may come from the kernel launched just before this one
+  griddep_wait();
 
   if (warp == 0) {
     // ------------------------------------------------------------- producer
@@ -525,6 +527,8 @@ __global__ void __launch_bounds__(GroupLayout<BN, STAGES, NACC, SPLIT, RS>::THRE
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // A and its scales may come from the kernel launched just before this one
+  griddep_wait();
 
   // With RS, registers move from warpgroup 0 (one TMA thread, one MMA thread) to
   // the epilogue warpgroups; the host launches this form only when the shares add
@@ -887,6 +891,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
+    // while the kernel launched before this one finishes, pull the first ring's weight
+    // slices into L2; every load into shared memory waits for that kernel (it may have
+    // written the weight as well as the tokens)
+    for (int j = 0; j < pre; ++j) tma_prefetch_l2_2d(&tmW, (kb0 + j) * BK, n0);
+    griddep_wait();
     for (int j = 0; j < pre; ++j) {
       mbar_arrive_expect_tx(&full[j], L::W_BYTES + L::X_BYTES);
       uint8_t* st = smem + j * (L::W_BYTES + L::X_BYTES);
@@ -903,6 +912,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  griddep_wait();   // A and its scales may come from the kernel launched just before
   float* part = reinterpret_cast<float*>(smem);   // [BT][128], valid after the mainloop
 
   if (warp == 0) {
@@ -1119,6 +1129,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
+    // the first ring's weight tiles into L2 while the kernel before this one finishes;
+    // the loads themselves wait for it
+    for (int j = 0; j < pre; ++j) tma_prefetch_l2_2d(&tmB, (kb0 + j) * BK, n0);
+    griddep_wait();
     for (int j = 0; j < pre; ++j) {
       mbar_arrive_expect_tx(&full[j], STAGE_BYTES);
       uint8_t* st = smem + j * STAGE_BYTES;
@@ -1134,6 +1148,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  griddep_wait();
   float* part = reinterpret_cast<float*>(smem);       // [rows][PSTRIDE], valid after the mainloop
 
   if (warp == 0) {
@@ -1267,6 +1282,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------- host side
 
+// Every GEMM is launched as a programmatic dependent of the work before it on the
+// stream: when that is a quant kernel (which lets its dependents launch early), the
+// GEMM's CTAs set up and start their weight loads while the quant finishes, and read
+// A and its scales only after griddepcontrol.wait.  cluster_x > 0 adds a cluster.
+template <typename Kern, typename... Args>
+cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t st, unsigned cluster_x,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  int n = 1;
+  if (cluster_x > 0) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster_x;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    n = 2;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 struct Config {
   int bn, stages;
   bool group_a;
@@ -1279,8 +1322,7 @@ cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorM
   auto kern = fp8_gemm_kernel<BN, STAGES>;
   const cudaError_t e = smem_opt_in(reinterpret_cast<const void*>(kern), L::ALLOC);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, L::ALLOC, st>>>(ta, tb, td, p);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), L::ALLOC, st, 0, ta, tb, td, p);
 }
 
 // Group-scale tiles: 128 x 256 with two accumulators and a register split (the
@@ -1314,11 +1356,8 @@ struct GroupKernels {
 
   static cudaError_t launch(bool use_split, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td,
                             const GemmArgs& p, int grid, cudaStream_t st) {
-    if (use_split)
-      split<<<grid, LS::THREADS, LS::ALLOC, st>>>(ta, tb, td, p);
-    else
-      alt<<<grid, LA::THREADS, LA::ALLOC, st>>>(ta, tb, td, p);
-    return cudaGetLastError();
+    if (use_split) return launch_pdl(split, dim3(grid), dim3(LS::THREADS), LS::ALLOC, st, 0, ta, tb, td, p);
+    return launch_pdl(alt, dim3(grid), dim3(LA::THREADS), LA::ALLOC, st, 0, ta, tb, td, p);
   }
 };
 
@@ -1359,19 +1398,9 @@ cudaError_t launch_swap(const CUtensorMap& tw, const CUtensorMap& tx, const Gemm
   SplitArgs sp;
   sp.splits = splits;
   sp.n_tiles = ceil_div(p.N, 128);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(sp.n_tiles * splits), static_cast<unsigned>(ceil_div(p.M, BT)), 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = L::ALLOC;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = static_cast<unsigned>(splits);
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, tw, tx, p, sp, static_cast<__nv_bfloat16*>(out));
+  return launch_pdl(kern, dim3(static_cast<unsigned>(sp.n_tiles * splits), static_cast<unsigned>(ceil_div(p.M, BT)), 1),
+                    dim3(kThreads), L::ALLOC, st, static_cast<unsigned>(splits), tw, tx, p, sp,
+                    static_cast<__nv_bfloat16*>(out));
 }
 
 // Split count for the small-M path: as many K slices (cluster size <= 8, at least two
@@ -1419,19 +1448,8 @@ cudaError_t launch_det_cluster(const CUtensorMap& ta, const CUtensorMap& tb, con
   auto kern = fp8_gemm_det_cluster_kernel<BN, STAGES>;
   const cudaError_t e = smem_opt_in(reinterpret_cast<const void*>(kern), L::ALLOC);
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(p.n_blocks * p.det_splits), static_cast<unsigned>(p.m_blocks), 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = L::ALLOC;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = static_cast<unsigned>(p.det_splits);
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, ta, tb, p, out);
+  return launch_pdl(kern, dim3(static_cast<unsigned>(p.n_blocks * p.det_splits), static_cast<unsigned>(p.m_blocks), 1),
+                    dim3(kThreads), L::ALLOC, st, static_cast<unsigned>(p.det_splits), ta, tb, p, out);
 }
 
 // The fold form of the deterministic split for each tile width: 128 x 256 with the
@@ -1471,8 +1489,7 @@ template <int BN>
 cudaError_t launch_det_fold(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td, const GemmArgs& p,
                             int grid, cudaStream_t st) {
   using F = DetFold<BN>;
-  F::kern<<<grid, F::L::THREADS, F::L::ALLOC, st>>>(ta, tb, td, p);
-  return cudaGetLastError();
+  return launch_pdl(F::kern, dim3(grid), dim3(F::L::THREADS), F::L::ALLOC, st, 0, ta, tb, td, p);
 }
 
 // Shape-keyed tile table.  Deterministic mode picks its tile from N alone, so every M

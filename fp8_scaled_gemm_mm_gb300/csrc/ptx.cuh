@@ -105,6 +105,15 @@ __device__ __forceinline__ void tma_load_2d_hint(const CUtensorMap* m, uint64_t*
       : "memory");
 }
 
+// Prefetch a 2-D tile into L2 (no shared memory written, no barrier): later loads of
+// the same tile hit L2.  L2 is the point of coherence, so a prefetch cannot leave a
+// stale copy behind if the data are written afterwards.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* m, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+               ::"l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y)
+               : "memory");
+}
+
 // Untiled bulk copy global -> shared (16-byte aligned addresses, size a multiple of 16),
 // completing as transaction bytes on `bar`.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -233,6 +242,19 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
 //   bit 15/16 A/B major (0 = K), bits 17-22 N >> 3, bits 24-28 M >> 4.
 __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int m, int n) {
   return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+// ------------------------------------------------- programmatic dependent launch
+
+// Wait until the grids this one depends on (launched before it on the stream, when it
+// was launched as a programmatic dependent) have completed and their memory is
+// visible; returns at once otherwise.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Let the grid that depends on this one start launching (its CTAs still wait for this
+// grid's completion before reading what it writes).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ------------------------------------------------------------------ clusters
