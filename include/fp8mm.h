@@ -37,6 +37,12 @@
  *    out the kernel records FP8MM_ETIMEOUT in a per-device status word, frees
  *    what it holds and returns.  fp8mm_get_device_status() reads that word.
  *  - `stream` is a cudaStream_t (0 = legacy default stream).
+ *  - fp8_scaled_mm launches its kernel as a programmatic dependent of the work
+ *    before it on the stream, and the quant kernels let such dependents start
+ *    early: after one of this library's quant kernels, the GEMM's CTAs set up
+ *    and prefetch weight tiles into L2 while the quant finishes, and read any
+ *    of their inputs only once it has completed (griddepcontrol.wait).  After
+ *    any other work the GEMM starts when that work ends, as usual.
  */
 #ifndef FP8MM_H_
 #define FP8MM_H_
