@@ -43,6 +43,7 @@ SHAPES = [(8320, 5376, 21504), (8320, 5376, 14336), (23216, 5376, 28672), (15760
 H100_TORCH_US = [1351.1, 896.4, 5295.9, 3570.9, 843.9]
 QUANT_M, QUANT_K = 8192, 7168
 FP8_OVER_BF16 = 2.0      # nominal dense FP8 : BF16 tensor rate on GB300 (4.5 : 2.25 PFLOP/s)
+NOMINAL_FP8_DENSE_TFLOPS = 4500.0   # GB300 dense FP8 tensor rate, nominal (context for the measured-peak fraction)
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
 L2_FLUSH_BYTES = 512 << 20
 
@@ -890,6 +891,8 @@ def main():
         "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights, bf16, quantized on device)",
         "config": workload_config(world),
         "gemm": {"tflops": round(gemm_tflops, 2), "ms_per_step": round(res["gemm_ms"], 4),
+                 "frac_of_measured_peak": round(gemm_tflops / fp8_peak, 4),
+                 "frac_of_nominal_dense_fp8": round(gemm_tflops / NOMINAL_FP8_DENSE_TFLOPS, 4),
                  "per_shape_tflops": [round(flops(*s) / (t * 1e-3) / 1e12, 1)
                                       for s, t in zip(SHAPES, res["per_shape_gemm_ms"])]},
         "roofline": {"bound": "tensor", "achieved": round(gemm_tflops, 2), "peak": round(fp8_peak, 1),
