@@ -287,7 +287,7 @@ def run_gpu(args, rank, world, local_rank):
     if rank == 0:
         quant_obj = bench_group_quant(torch, fm, synth, dev, flush)
 
-    widened = per_tensor = determ = scatter = sweep = tiny = decode = None
+    widened = per_tensor = determ = scatter = sweep = tiny = decode = chain = None
     if rank == 0:
         peaks, _ = load_peaks()
         scatter = bench_scatter(torch, fm, synth, dev, flush)
@@ -297,6 +297,7 @@ def run_gpu(args, rank, world, local_rank):
         per_tensor = bench_per_tensor(torch, fm, dev, flush)
         determ = bench_deterministic(torch, fm, dev, flush)
         decode = bench_decode_step(torch, fm, synth, dev, flush, peaks["hbm_gbs"])
+        chain = bench_decode_chain(torch, fm, dev, flush, peaks["hbm_gbs"])
 
     # ---- end to end through the C ABI with host buffers
     e2e = None
@@ -306,7 +307,7 @@ def run_gpu(args, rank, world, local_rank):
     res = dict(step_ms=tot_step_ms / args.steps, gemm_ms=tot_gemm_ms / args.steps,
                quant_ms=tot_quant_ms / args.steps, wall=wall, step_flops=step_flops,
                step_quant_bytes=step_quant_bytes, clocks=clocks, quant=quant_obj, e2e=e2e, widened=widened,
-               per_tensor=per_tensor, determ=determ, scatter=scatter, sweep=sweep, tiny=tiny, decode=decode,
+               per_tensor=per_tensor, determ=determ, scatter=scatter, sweep=sweep, tiny=tiny, decode=decode, chain=chain,
                per_shape_gemm_ms=[x / args.steps for x in per_shape_gemm], launches=2 * len(work) * args.steps)
     return res
 
@@ -572,6 +573,57 @@ def bench_decode_step(torch, fm, synth, dev, flush, hbm_peak, reps=10):
                         "frac": round(nbytes / (t_pair * 1e-6) / 1e9 / hbm_peak, 4)})
             del x, A, a_s, D
         del B, b_s
+    return out
+
+
+def bench_decode_chain(torch, fm, dev, flush, hbm_peak, layers=16, reps=10):
+    """A decode step's chain of GEMMs, K = 4096: x [M, K] against `layers` distinct
+    per-tensor-scaled E4M3 weights [N, K] (layers x N x K bytes, far beyond L2),
+    launched back to back and replayed from one CUDA graph; each GEMM is a
+    programmatic dependent of the one before, whose early trigger lets it set up and
+    prefetch weight tiles while that one finishes.  Per-GEMM time = replay time /
+    layers (L2 evicted before each replay); bytes per GEMM: weight, x and the bf16
+    output."""
+    K = 4096
+    g = torch.Generator(device=dev).manual_seed(17)
+    out = []
+    for N in (4096, 14336):
+        Ws = [torch.randint(0, 126, (N, K), generator=g, dtype=torch.uint8, device=dev) for _ in range(layers)]
+        for M in (1, 16):
+            x = torch.randint(0, 126, (M, K), generator=g, dtype=torch.uint8, device=dev)
+            a_s = torch.full((1,), 0.02, dtype=torch.float32, device=dev)
+            b_s = torch.full((1,), 0.001, dtype=torch.float32, device=dev)
+            outs = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for _ in range(layers)]
+            st = torch.cuda.Stream()
+            st.wait_stream(torch.cuda.current_stream())
+
+            def chain(stream):
+                for i in range(layers):
+                    fm.fp8_scaled_mm(x, Ws[i], a_s, b_s, fm.A_TENSOR | fm.B_TENSOR, outs[i], stream=stream)
+            with torch.cuda.stream(st):
+                chain(st)                 # set-up outside the capture
+                st.synchronize()
+                graph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(graph, stream=st):
+                    chain(torch.cuda.current_stream())
+            torch.cuda.synchronize()
+            ts = []
+            for _ in range(reps):
+                flush()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                graph.replay()
+                b.record()
+                torch.cuda.synchronize()
+                ts.append(a.elapsed_time(b) * 1e3)
+            us = statistics.median(ts) / layers
+            nbytes = N * K + M * K + 2 * M * N
+            out.append({"M": M, "N": N, "K": K, "layers": layers, "us_per_gemm": round(us, 2),
+                        "gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
+                        "frac": round(nbytes / (us * 1e-6) / 1e9 / hbm_peak, 4)})
+            del graph, x, outs
+        del Ws
+        torch.cuda.empty_cache()
     return out
 
 
@@ -936,6 +988,11 @@ def main():
                                              "programmatic dependent of the quant) and each alone; L2 flushed "
                                              "before each; frac of the HBM peak for the pair's bytes",
                                      "shapes": res["decode"]}
+    if res.get("chain"):
+        line["decode_chain_k4096"] = {"note": "16 decode GEMMs (distinct per-tensor-scaled weights) back to back in one "
+                                              "CUDA graph, each a programmatic dependent of the one before; per-GEMM "
+                                              "time, L2 evicted before each replay; frac of HBM",
+                                      "shapes": res["chain"]}
     if res["widened"]:
         wd = res["widened"]
         for k, v in wd.items():

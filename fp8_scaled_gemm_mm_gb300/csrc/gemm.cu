@@ -854,6 +854,10 @@ template <int BT>
 __global__ void __launch_bounds__(kThreads, 1)
     fp8_gemm_swap_splitk_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                                 const GemmArgs p, const SplitArgs sp, __nv_bfloat16* out) {
+  // A kernel launched after this one on the stream as a programmatic dependent (the
+  // next GEMM of a decode step) may start its set-up and its weight prefetch now; it
+  // reads what this kernel writes only after griddepcontrol.wait
+  griddep_launch_dependents();
   using L = SwapLayout<BT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -1096,6 +1100,7 @@ template <int BN, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
     fp8_gemm_det_cluster_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                                 const GemmArgs p, void* out) {
+  griddep_launch_dependents();   // as in the small-M kernel
   using L = DetLayout<BN, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);

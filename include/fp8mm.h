@@ -41,8 +41,11 @@
  *    before it on the stream, and the quant kernels let such dependents start
  *    early: after one of this library's quant kernels, the GEMM's CTAs set up
  *    and prefetch weight tiles into L2 while the quant finishes, and read any
- *    of their inputs only once it has completed (griddepcontrol.wait).  After
- *    any other work the GEMM starts when that work ends, as usual.
+ *    of their inputs only once it has completed (griddepcontrol.wait).  The
+ *    small-M (M <= 128) and the deterministic cluster GEMMs let the next GEMM
+ *    start early in the same way, so a chain of decode GEMMs overlaps each
+ *    one's set-up with the end of the one before.  After any other work the
+ *    GEMM starts when that work ends, as usual.
  */
 #ifndef FP8MM_H_
 #define FP8MM_H_
