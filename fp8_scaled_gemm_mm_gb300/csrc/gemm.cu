@@ -65,6 +65,10 @@ struct GemmArgs {
   int out_fp16;
   int det_splits;   // deterministic mode: K ranges summed in order (1 = no split)
   int* status;
+  // Limit of the pipeline's waits (stage, accumulator and cluster hand-offs).  The
+  // drains -- a producer waiting for its last loads, the MMA thread for its last
+  // MMAs -- always keep the full kWaitTimeoutNs: every copy and MMA in flight must
+  // have landed before a CTA releases TMEM or exits, whatever this limit is.
   uint64_t timeout_ns;
 };
 
@@ -278,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ph ^= 1u;
         }
         volatile int never = 0;
-        mbar_wait(&full[s], ph, &never, p.status, p.timeout_ns);
+        mbar_wait(&full[s], ph, &never, p.status, kWaitTimeoutNs);
       }
     }
   } else if (warp == 1) {
@@ -321,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // All MMAs issued here must be complete before TMEM is released.
       mma_commit(drain);
       volatile int never = 0;
-      mbar_wait(drain, 0, &never, p.status, p.timeout_ns);
+      mbar_wait(drain, 0, &never, p.status, kWaitTimeoutNs);
     }
   } else {
     // ------------------------------------------------------------- epilogue
@@ -564,7 +568,7 @@ __global__ void __launch_bounds__(GroupLayout<BN, STAGES, NACC, SPLIT, RS>::THRE
           ph ^= 1u;
         }
         volatile int never = 0;
-        mbar_wait(&full[s], ph, &never, p.status, p.timeout_ns);
+        mbar_wait(&full[s], ph, &never, p.status, kWaitTimeoutNs);
       }
     }
   } else if (warp == 1) {
@@ -605,7 +609,7 @@ __global__ void __launch_bounds__(GroupLayout<BN, STAGES, NACC, SPLIT, RS>::THRE
       }
       mma_commit(drain);
       volatile int never = 0;
-      mbar_wait(drain, 0, &never, p.status, p.timeout_ns);
+      mbar_wait(drain, 0, &never, p.status, kWaitTimeoutNs);
     } else if (lane == 0) {
       constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
       uint32_t stage = 0, phase = 0, acc_i = 0;
@@ -637,7 +641,7 @@ __global__ void __launch_bounds__(GroupLayout<BN, STAGES, NACC, SPLIT, RS>::THRE
       }
       mma_commit(drain);
       volatile int never = 0;
-      mbar_wait(drain, 0, &never, p.status, p.timeout_ns);
+      mbar_wait(drain, 0, &never, p.status, kWaitTimeoutNs);
     }
   }
   } else {
@@ -944,7 +948,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ph ^= 1u;
         }
         volatile int never = 0;
-        mbar_wait(&full[s], ph, &never, p.status, p.timeout_ns);
+        mbar_wait(&full[s], ph, &never, p.status, kWaitTimeoutNs);
       }
     }
   } else if (warp == 1) {
@@ -970,7 +974,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(tfull);
       mma_commit(drain);
       volatile int never = 0;
-      mbar_wait(drain, 0, &never, p.status, p.timeout_ns);
+      mbar_wait(drain, 0, &never, p.status, kWaitTimeoutNs);
     }
   } else {
     {
@@ -1181,7 +1185,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ph ^= 1u;
         }
         volatile int never = 0;
-        mbar_wait(&full[s], ph, &never, p.status, p.timeout_ns);
+        mbar_wait(&full[s], ph, &never, p.status, kWaitTimeoutNs);
       }
     }
   } else if (warp == 1) {
@@ -1207,7 +1211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(tfull);
       mma_commit(drain);
       volatile int never = 0;
-      mbar_wait(drain, 0, &never, p.status, p.timeout_ns);
+      mbar_wait(drain, 0, &never, p.status, kWaitTimeoutNs);
     }
   } else {
     // TMEM -> own partial: lane = row within the tile; the valid rows only
@@ -1585,7 +1589,7 @@ extern "C" int fp8_scaled_mm(const void* A, const void* B, const float* a_scale,
   p.out_fp16 = out_dtype == FP8MM_DTYPE_FP16;
   p.det_splits = 1;
   p.status = status;
-  p.timeout_ns = kWaitTimeoutNs;
+  p.timeout_ns = gemm_wait_timeout_ns();
 
   if (deterministic && !group_a) {
     // batch-invariant split: the tile width from N, the K ranges from N and K; the

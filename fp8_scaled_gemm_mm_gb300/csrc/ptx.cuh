@@ -63,7 +63,8 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
 }
 
 // Wait until the phase with parity `parity` of `bar` has completed.  Waiting
-// threads are suspended in hardware between checks rather than spinning.
+// threads are suspended in hardware between checks rather than spinning (for at
+// most 100 us, or `timeout_ns` if that is shorter, at a time).
 // Bounded: gives up after `timeout_ns` of global time or when *abort becomes
 // non-zero, records `code` in *status (first error wins) and sets *abort.
 // Returns false if it gave up.
@@ -72,8 +73,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
+  const uint32_t hint = timeout_ns < 100000u ? static_cast<uint32_t>(timeout_ns) : 100000u;
   for (;;) {
-    if (mbar_try_wait_sleep(a, parity, 100000u)) return true;
+    if (mbar_try_wait_sleep(a, parity, hint)) return true;
     if (*abort) return false;
     if (globaltimer_ns() - t0 > timeout_ns) {
       if (status) atomicCAS(status, 0, code);
