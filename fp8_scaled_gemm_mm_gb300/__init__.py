@@ -77,8 +77,8 @@ def lib():
         L.fp8mm_get_device_status.restype = I
         L.fp8mm_selftest_bounded_wait.argtypes = [I64, P]
         L.fp8mm_selftest_bounded_wait.restype = I
-        L.fp8mm_set_gemm_wait_timeout_ns.argtypes = [I64]
-        L.fp8mm_set_gemm_wait_timeout_ns.restype = I
+        L.fp8mm_set_wait_timeout_ns.argtypes = [I64]
+        L.fp8mm_set_wait_timeout_ns.restype = I
         L.fp8mm_selftest_scale_math.argtypes = [ctypes.c_uint32, ctypes.c_uint32, P, P]
         L.fp8mm_selftest_scale_math.restype = I
         L.fp8mm_status_string.argtypes = [I]
@@ -286,6 +286,7 @@ def selftest_bounded_wait(timeout_ns: int, stream=None):
     _check(lib().fp8mm_selftest_bounded_wait(int(timeout_ns), _stream(stream)), "fp8mm_selftest_bounded_wait")
 
 
-def set_gemm_wait_timeout_ns(timeout_ns: int):
-    """Limit of the GEMM kernels' pipeline waits for later launches (0: the default)."""
-    _check(lib().fp8mm_set_gemm_wait_timeout_ns(int(timeout_ns)), "fp8mm_set_gemm_wait_timeout_ns")
+def set_wait_timeout_ns(timeout_ns: int):
+    """Limit of the GEMM and group-quant kernels' pipeline waits for later launches
+    (0: the default)."""
+    _check(lib().fp8mm_set_wait_timeout_ns(int(timeout_ns)), "fp8mm_set_wait_timeout_ns")

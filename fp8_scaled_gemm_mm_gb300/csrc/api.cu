@@ -23,10 +23,10 @@ int g_sms[kMaxDevices] = {};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::mutex g_once_mu;   // separate from g_mu: set-ups may call num_sms() and the like
 std::map<std::pair<const void*, int>, int> g_once;
-std::atomic<uint64_t> g_gemm_wait_ns{kWaitTimeoutNs};
+std::atomic<uint64_t> g_wait_ns{kWaitTimeoutNs};
 }  // namespace
 
-uint64_t gemm_wait_timeout_ns() { return g_gemm_wait_ns.load(std::memory_order_relaxed); }
+uint64_t wait_timeout_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
 
 int once_per_device(const void* key, const std::function<int()>& setup) {
   int dev = 0;
@@ -137,9 +137,9 @@ extern "C" int fp8mm_selftest_bounded_wait(int64_t timeout_ns, fp8mm_stream_t st
   return cudaGetLastError() == cudaSuccess ? FP8MM_OK : FP8MM_ECUDA;
 }
 
-extern "C" int fp8mm_set_gemm_wait_timeout_ns(int64_t timeout_ns) {
+extern "C" int fp8mm_set_wait_timeout_ns(int64_t timeout_ns) {
   if (timeout_ns < 0 || timeout_ns > static_cast<int64_t>(kWaitTimeoutNs)) return FP8MM_EINVAL;
-  g_gemm_wait_ns.store(timeout_ns == 0 ? kWaitTimeoutNs : static_cast<uint64_t>(timeout_ns),
+  g_wait_ns.store(timeout_ns == 0 ? kWaitTimeoutNs : static_cast<uint64_t>(timeout_ns),
                        std::memory_order_relaxed);
   return FP8MM_OK;
 }

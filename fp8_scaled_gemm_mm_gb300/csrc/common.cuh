@@ -44,8 +44,8 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 // Upper bound on any single in-kernel wait before it gives up (ns).
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
 
-// Limit of the GEMM kernels' pipeline waits for launches from now on: kWaitTimeoutNs
-// unless fp8mm_set_gemm_wait_timeout_ns set another (defined in api.cu).
-uint64_t gemm_wait_timeout_ns();
+// Limit of the pipeline waits of the GEMM and group-quant kernels launched from now
+// on: kWaitTimeoutNs unless fp8mm_set_wait_timeout_ns set another (defined in api.cu).
+uint64_t wait_timeout_ns();
 
 }  // namespace fp8mm

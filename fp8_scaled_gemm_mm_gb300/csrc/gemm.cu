@@ -1589,7 +1589,7 @@ extern "C" int fp8_scaled_mm(const void* A, const void* B, const float* a_scale,
   p.out_fp16 = out_dtype == FP8MM_DTYPE_FP16;
   p.det_splits = 1;
   p.status = status;
-  p.timeout_ns = gemm_wait_timeout_ns();
+  p.timeout_ns = wait_timeout_ns();
 
   if (deterministic && !group_a) {
     // batch-invariant split: the tile width from N, the K ranges from N and K; the

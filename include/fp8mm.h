@@ -277,18 +277,19 @@ FP8MM_API int fp8mm_get_device_status(int device, int clear);
 FP8MM_API int fp8mm_selftest_bounded_wait(int64_t timeout_ns, fp8mm_stream_t stream);
 
 /*
- * Diagnostic: the limit, in ns, of the waits inside the GEMM kernels' pipelines
- * (stage, accumulator and cluster hand-offs) for every fp8_scaled_mm launched
- * after this call, process-wide; 0 restores the default (2 s, also the most
- * allowed).  A short limit makes real waits give up mid-run: the kernel then
- * records FP8MM_ETIMEOUT, leaves every output tile it had not finished
- * unwritten, waits (with the full limit) for its own copies and MMAs in flight,
- * frees its TMEM and returns -- the path a fault in production would take,
- * exercised without one.  The quant kernels keep the default.  Returns
- * FP8MM_EINVAL for a negative or larger value; not for use while other host
- * threads launch GEMMs that expect the default.
+ * Diagnostic: the limit, in ns, of the waits inside the pipelines of the GEMM
+ * kernels (stage, accumulator and cluster hand-offs) and of the group-quant
+ * kernel (stage hand-offs) for every launch after this call, process-wide; 0
+ * restores the default (2 s, also the most allowed).  A short limit makes real
+ * waits give up mid-run: the kernel then records FP8MM_ETIMEOUT, leaves every
+ * output it had not finished unwritten (GEMM tiles; the quant's items of up to
+ * 32 rows x 512 columns), waits with the full limit for its own copies and MMAs
+ * in flight, frees its TMEM and returns -- the path a fault in production would
+ * take, exercised without one.  Returns FP8MM_EINVAL for a negative or larger
+ * value; not for use while other host threads launch kernels that expect the
+ * default.
  */
-FP8MM_API int fp8mm_set_gemm_wait_timeout_ns(int64_t timeout_ns);
+FP8MM_API int fp8mm_set_wait_timeout_ns(int64_t timeout_ns);
 
 /*
  * Diagnostic: evaluate the quant kernels' per-group scale arithmetic for every

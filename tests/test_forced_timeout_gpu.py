@@ -1,12 +1,13 @@
-"""Forced timeouts inside the real GEMM kernels: failure detection without a GPU fault.
+"""Forced timeouts inside the real kernels: failure detection without a GPU fault.
 
-fp8mm_set_gemm_wait_timeout_ns shortens the limit of the GEMM pipelines' bounded
-waits, so that real waits -- for a stage's TMA loads, for an accumulator, for a
-cluster peer -- give up in mid-run.  For every kernel form and several limits:
+fp8mm_set_wait_timeout_ns shortens the limit of the GEMM and group-quant
+pipelines' bounded waits, so that real waits -- for a stage's TMA loads, for an
+accumulator, for a cluster peer -- give up in mid-run.  For every GEMM form, the
+group quant (plain and fused) and several limits:
 the call returns; the device status word reads FP8MM_ETIMEOUT (or FP8MM_OK if no
 wait outlasted the limit); every output element is either still the sentinel the
 buffer was filled with or the correct value (a kernel that gives up leaves the
-tiles it had not finished unwritten); and the next call, with the default limit,
+tiles or items it had not finished unwritten); and the next call, with the default limit,
 is correct and clean (the context survives).  The drains -- a producer waiting
 for its own loads, an MMA thread for its own MMAs -- keep the full limit, so no
 copy or MMA is still in flight when a CTA frees its TMEM or exits."""
@@ -43,7 +44,7 @@ CASES = [
 @pytest.fixture(autouse=True)
 def _default_limit_after():
     yield
-    fm.set_gemm_wait_timeout_ns(0)
+    fm.set_wait_timeout_ns(0)
 
 
 def _run(M, N, K, out_dtype, launch):
@@ -81,9 +82,9 @@ def test_short_wait_limit_gives_up_cleanly(case):
     assert fm.get_device_status(clear=True) == fm.OK
     outcomes = []
     for limit in LIMITS_NS:
-        fm.set_gemm_wait_timeout_ns(limit)
+        fm.set_wait_timeout_ns(limit)
         out, status = _run(M, N, K, out_dtype, launch)
-        fm.set_gemm_wait_timeout_ns(0)
+        fm.set_wait_timeout_ns(0)
         assert status in (fm.OK, fm.ETIMEOUT), (limit, status)
         n = _check_written(out, exact, sumabs, K, out_dtype, f"limit {limit} ns")
         if status == fm.OK:
@@ -97,10 +98,50 @@ def test_short_wait_limit_gives_up_cleanly(case):
     check_gemm(bits(out), exact, sumabs, K, out_dtype, "after the forced timeouts")
 
 
+QSENT = 0x5A
+
+
+@pytest.mark.parametrize("fuse", [False, True])
+@pytest.mark.parametrize("fmt,colmajor", [(0, False), (2, True)])
+def test_quant_short_wait_limit_gives_up_cleanly(fuse, fmt, colmajor):
+    dev = require_gpu()
+    M, K = 4096, 7168
+    x = synth.quant_input(M, 2 * K if fuse else K, torch.bfloat16, seed=77)
+    q_ref, s_ref = oracle.group_quant(synth.to_bits(x), 0, 128, fmt, colmajor, fuse)
+    s_ref = s_ref.view(np.uint32)
+    xd = x.to(dev)
+
+    def run():
+        q = torch.full((M, K), QSENT, dtype=torch.uint8, device=dev)
+        s = torch.empty(fm.scale_shape(M, K, 128, fmt, colmajor), dtype=fm.scale_dtype(fmt), device=dev)
+        s.view(torch.uint8).fill_(QSENT)
+        fm.per_token_group_quant_fp8(xd, q, s, 128, fmt, colmajor, fuse)
+        torch.cuda.synchronize()
+        return bits(q), bits(s).view(np.uint32), fm.get_device_status(clear=True)
+
+    assert fm.get_device_status(clear=True) == fm.OK
+    statuses = []
+    for limit in LIMITS_NS:
+        fm.set_wait_timeout_ns(limit)
+        qg, sg, status = run()
+        fm.set_wait_timeout_ns(0)
+        assert status in (fm.OK, fm.ETIMEOUT), (limit, status)
+        assert np.all((qg == q_ref) | (qg == QSENT)), f"limit {limit} ns: wrong codes written"
+        assert np.all((sg == s_ref) | (sg == 0x5A5A5A5A)), f"limit {limit} ns: wrong scales written"
+        if status == fm.OK:
+            assert np.array_equal(qg, q_ref)
+        statuses.append(status)
+    assert statuses[0] == fm.ETIMEOUT, statuses
+    qg, sg, status = run()
+    assert status == fm.OK and np.array_equal(qg, q_ref)
+    padded = sg != 0x5A5A5A5A
+    assert np.array_equal(sg[padded], s_ref[padded])
+
+
 def test_wait_limit_argument_checks():
     require_gpu()
     with pytest.raises(fm.Fp8mmError):
-        fm.set_gemm_wait_timeout_ns(-1)
+        fm.set_wait_timeout_ns(-1)
     with pytest.raises(fm.Fp8mmError):
-        fm.set_gemm_wait_timeout_ns(3_000_000_000)
-    fm.set_gemm_wait_timeout_ns(0)
+        fm.set_wait_timeout_ns(3_000_000_000)
+    fm.set_wait_timeout_ns(0)
