@@ -119,6 +119,17 @@ def test_masked_and_new_entry_validation(L):
     assert rq(f, f, f, ctypes.cast(w, ctypes.c_void_p), 0, 8, 32, f, None) == -1   # no shards
 
 
+def test_wait_limit_setting_validation(L):
+    # host-side only: a negative limit or one above the 2 s default is rejected;
+    # 0 restores the default
+    L.fp8mm_set_wait_timeout_ns.argtypes = [ctypes.c_int64]
+    assert L.fp8mm_set_wait_timeout_ns(-1) == -1
+    assert L.fp8mm_set_wait_timeout_ns(2_000_000_001) == -1
+    assert L.fp8mm_set_wait_timeout_ns(1000) == 0
+    assert L.fp8mm_set_wait_timeout_ns(2_000_000_000) == 0
+    assert L.fp8mm_set_wait_timeout_ns(0) == 0
+
+
 def test_plain_c_consumer(L, tmp_path):
     # the header compiles as C11 and a C program links the library and gets the
     # documented statuses back (host-side paths only)
