@@ -287,7 +287,7 @@ def run_gpu(args, rank, world, local_rank):
     if rank == 0:
         quant_obj = bench_group_quant(torch, fm, synth, dev, flush)
 
-    widened = per_tensor = determ = scatter = sweep = tiny = decode = chain = None
+    widened = per_tensor = determ = scatter = sweep = tiny = decode = chain = layers_obj = None
     if rank == 0:
         peaks, _ = load_peaks()
         scatter = bench_scatter(torch, fm, synth, dev, flush)
@@ -298,6 +298,7 @@ def run_gpu(args, rank, world, local_rank):
         determ = bench_deterministic(torch, fm, dev, flush)
         decode = bench_decode_step(torch, fm, synth, dev, flush, peaks["hbm_gbs"])
         chain = bench_decode_chain(torch, fm, dev, flush, peaks["hbm_gbs"])
+        layers_obj = bench_decode_layers(torch, fm, dev, flush, peaks["hbm_gbs"])
 
     # ---- end to end through the C ABI with host buffers
     e2e = None
@@ -307,7 +308,7 @@ def run_gpu(args, rank, world, local_rank):
     res = dict(step_ms=tot_step_ms / args.steps, gemm_ms=tot_gemm_ms / args.steps,
                quant_ms=tot_quant_ms / args.steps, wall=wall, step_flops=step_flops,
                step_quant_bytes=step_quant_bytes, clocks=clocks, quant=quant_obj, e2e=e2e, widened=widened,
-               per_tensor=per_tensor, determ=determ, scatter=scatter, sweep=sweep, tiny=tiny, decode=decode, chain=chain,
+               per_tensor=per_tensor, determ=determ, scatter=scatter, sweep=sweep, tiny=tiny, decode=decode, chain=chain, layers=layers_obj,
                per_shape_gemm_ms=[x / args.steps for x in per_shape_gemm], launches=2 * len(work) * args.steps)
     return res
 
@@ -622,6 +623,59 @@ def bench_decode_chain(torch, fm, dev, flush, hbm_peak, layers=16, reps=10):
                         "gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
                         "frac": round(nbytes / (us * 1e-6) / 1e9 / hbm_peak, 4)})
             del graph, x, outs
+        del Ws
+        torch.cuda.empty_cache()
+    return out
+
+
+def bench_decode_layers(torch, fm, dev, flush, hbm_peak, layers=16, reps=10):
+    """A decode step's chain of linear layers, K = 4096: per layer the per-token quant
+    of its activation x_i [M, K] bf16 (one fp32 scale per row) and the rowwise GEMM
+    against its own per-channel E4M3 weight [N, K]; `layers` layers back to back,
+    replayed from one CUDA graph, every kernel a programmatic dependent of the one
+    before.  Per-layer time = replay time / layers (L2 evicted before each replay);
+    bytes per layer: x read, codes and scales written and read back, the weight and
+    the bf16 output."""
+    K = 4096
+    g = torch.Generator(device=dev).manual_seed(23)
+    out = []
+    for N in (4096, 14336):
+        Ws = [torch.randint(0, 126, (N, K), generator=g, dtype=torch.uint8, device=dev) for _ in range(layers)]
+        bs = torch.full((N, 1), 0.001, dtype=torch.float32, device=dev)
+        for M in (1, 16):
+            xs = [torch.randn((M, K), generator=g, device=dev).to(torch.bfloat16) for _ in range(layers)]
+            As = [torch.empty((M, K), dtype=torch.uint8, device=dev) for _ in range(layers)]
+            ass = [torch.empty((M, 1), dtype=torch.float32, device=dev) for _ in range(layers)]
+            outs = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for _ in range(layers)]
+            st = torch.cuda.Stream()
+            st.wait_stream(torch.cuda.current_stream())
+
+            def chain(stream):
+                for i in range(layers):
+                    fm.per_token_group_quant_fp8(xs[i], As[i], ass[i], K, stream=stream)
+                    fm.fp8_scaled_mm(As[i], Ws[i], ass[i], bs, fm.A_ROW | fm.B_COL, outs[i], stream=stream)
+            with torch.cuda.stream(st):
+                chain(st)                 # set-up outside the capture
+                st.synchronize()
+                graph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(graph, stream=st):
+                    chain(torch.cuda.current_stream())
+            torch.cuda.synchronize()
+            ts = []
+            for _ in range(reps):
+                flush()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                graph.replay()
+                b.record()
+                torch.cuda.synchronize()
+                ts.append(a.elapsed_time(b) * 1e3)
+            us = statistics.median(ts) / layers
+            nbytes = 2 * M * K + 2 * (M * K + 4 * M) + N * K + 4 * N + 2 * M * N
+            out.append({"M": M, "N": N, "K": K, "layers": layers, "us_per_layer": round(us, 2),
+                        "gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
+                        "frac": round(nbytes / (us * 1e-6) / 1e9 / hbm_peak, 4)})
+            del graph, xs, As, ass, outs
         del Ws
         torch.cuda.empty_cache()
     return out
@@ -993,6 +1047,11 @@ def main():
                                               "CUDA graph, each a programmatic dependent of the one before; per-GEMM "
                                               "time, L2 evicted before each replay; frac of HBM",
                                       "shapes": res["chain"]}
+    if res.get("layers"):
+        line["decode_layers_k4096"] = {"note": "16 decode layers (per-token quant + rowwise GEMM, own weights) back to "
+                                               "back in one CUDA graph, every kernel a programmatic dependent of the one "
+                                               "before; per-layer time, L2 evicted before each replay; frac of HBM",
+                                       "shapes": res["layers"]}
     if res["widened"]:
         wd = res["widened"]
         for k, v in wd.items():

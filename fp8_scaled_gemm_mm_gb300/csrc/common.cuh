@@ -41,6 +41,36 @@ inline cudaError_t smem_opt_in(const void* kernel, int bytes) {
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Launch `kern` as a programmatic dependent of the work before it on the stream: its
+// CTAs may start (set up, prefetch into L2) once that work lets its dependents launch,
+// and read anything it produced only after griddepcontrol.wait, which every kernel
+// launched this way executes first.  Every GEMM and the group / per-token quant
+// kernels are launched so; the quant kernels and the small-M GEMMs let their own
+// dependents launch when they start.  cluster_x > 0 adds a cluster of that size.
+template <typename Kern, typename... Args>
+cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t st, unsigned cluster_x,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  int n = 1;
+  if (cluster_x > 0) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster_x;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    n = 2;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // Upper bound on any single in-kernel wait before it gives up (ns).
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
 

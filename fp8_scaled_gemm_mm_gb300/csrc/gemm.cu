@@ -1291,34 +1291,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------- host side
 
-// Every GEMM is launched as a programmatic dependent of the work before it on the
-// stream: when that is a quant kernel (which lets its dependents launch early), the
-// GEMM's CTAs set up and start their weight loads while the quant finishes, and read
-// A and its scales only after griddepcontrol.wait.  cluster_x > 0 adds a cluster.
-template <typename Kern, typename... Args>
-cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t st, unsigned cluster_x,
-                       Args... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  int n = 1;
-  if (cluster_x > 0) {
-    attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = cluster_x;
-    attr[1].val.clusterDim.y = 1;
-    attr[1].val.clusterDim.z = 1;
-    n = 2;
-  }
-  cfg.attrs = attr;
-  cfg.numAttrs = n;
-  return cudaLaunchKernelEx(&cfg, kern, args...);
-}
-
 struct Config {
   int bn, stages;
   bool group_a;

@@ -37,15 +37,16 @@
  *    out the kernel records FP8MM_ETIMEOUT in a per-device status word, frees
  *    what it holds and returns.  fp8mm_get_device_status() reads that word.
  *  - `stream` is a cudaStream_t (0 = legacy default stream).
- *  - fp8_scaled_mm launches its kernel as a programmatic dependent of the work
- *    before it on the stream, and the quant kernels let such dependents start
- *    early: after one of this library's quant kernels, the GEMM's CTAs set up
- *    and prefetch weight tiles into L2 while the quant finishes, and read any
- *    of their inputs only once it has completed (griddepcontrol.wait).  The
- *    small-M (M <= 128) and the deterministic cluster GEMMs let the next GEMM
- *    start early in the same way, so a chain of decode GEMMs overlaps each
- *    one's set-up with the end of the one before.  After any other work the
- *    GEMM starts when that work ends, as usual.
+ *  - fp8_scaled_mm and the group / per-token quant entry points
+ *    (per_token_group_quant_fp8 and its scatter, masked, int8 and row-padded
+ *    forms) launch their kernels as programmatic dependents of the work before
+ *    them on the stream: when that work lets its dependents start early, their
+ *    CTAs launch and set up while it finishes, and read or write anything only
+ *    once it has completed (griddepcontrol.wait).  The quant kernels, the
+ *    static quant and the small-M (M <= 128) and deterministic cluster GEMMs
+ *    let their own dependents start when they start, so in a decode step each
+ *    kernel's launch and set-up overlap the end of the one before.  After any
+ *    other work the kernel starts when that work ends, as usual.
  */
 #ifndef FP8MM_H_
 #define FP8MM_H_
