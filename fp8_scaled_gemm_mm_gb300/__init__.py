@@ -7,9 +7,27 @@ library's CUDA kernels; there is no other implementation to fall back to, and
 importing this module fails loudly if the library has not been built.
 
 Operations (see the header for full semantics):
-  per_token_group_quant_fp8          bf16/fp16 -> E4M3FN codes + scales
-  per_token_group_quant_fp8_scatter  the same, written to topk destination rows
-  fp8_scaled_mm                      out = round(a_s * b_s * A B^T (+ bias))
+  per_token_group_quant_fp8             bf16/fp16 -> E4M3FN codes + scales (group 32/64/128 or
+                                        the whole row; fp32, pow-2 or packed UE8M0 scales; fused
+                                        SiLU(gate) * up)
+  per_token_group_quant_fp8_scatter     the same, written to topk destination rows
+  silu_and_mul_masked_post_quant_fp8    fused quant of the expert-major [E, T, 2K] layout
+  per_token_group_quant_int8            int8 codes with fp32 scales
+  per_token_group_quant_fp8_row_padded  outputs sized for M_pad >= M rows, tail rows zeroed
+  static_per_tensor_quant_fp8           E4M3(x / s) with a given scale
+  requantize_with_max_scale_fp8         a fused weight's shards brought to their largest scale
+  fp8_scaled_mm                         out = round(a_s * b_s * A B^T (+ bias)); per-tensor,
+                                        per-row/column, group-128 A and 128 x 128 block B scales;
+                                        deterministic (batch-invariant) mode
+Diagnostics: get_device_status, selftest_bounded_wait, selftest_scale_math,
+set_wait_timeout_ns.
+
+Every call is asynchronous on the given stream (default: torch's current one);
+buffers are the caller's, the library allocates nothing per call.
+
+    q, s = fm.alloc_group_quant_outputs(M, K, 128, fm.SCALE_UE8M0_PACKED, True, device="cuda")
+    fm.per_token_group_quant_fp8(x, q, s, 128, fm.SCALE_UE8M0_PACKED, True)
+    fm.fp8_scaled_mm(q, w_codes, s, w_block_scales, fm.A_GROUP128_UE8M0 | fm.B_BLOCK128, out)
 """
 import ctypes
 import os
@@ -20,7 +38,8 @@ __all__ = [
     "Fp8mmError", "lib", "per_token_group_quant_fp8", "per_token_group_quant_fp8_scatter",
     "fp8_scaled_mm", "silu_and_mul_masked_post_quant_fp8", "static_per_tensor_quant_fp8",
     "per_token_group_quant_int8", "per_token_group_quant_fp8_row_padded",
-    "requantize_with_max_scale_fp8", "masked_scale_shape", "get_device_status", "selftest_bounded_wait", "selftest_scale_math", "scale_shape", "scale_dtype",
+    "requantize_with_max_scale_fp8", "masked_scale_shape", "get_device_status", "selftest_bounded_wait",
+    "selftest_scale_math", "set_wait_timeout_ns", "scale_shape", "scale_dtype",
     "alloc_group_quant_outputs", "SCALE_FP32", "SCALE_FP32_POW2", "SCALE_UE8M0_PACKED",
     "A_TENSOR", "A_ROW", "A_GROUP128", "A_GROUP128_COLMAJOR", "A_GROUP128_UE8M0", "B_TENSOR", "B_COL",
     "B_BLOCK128",
