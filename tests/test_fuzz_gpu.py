@@ -82,3 +82,48 @@ def test_quant_fuzz(M, K, group, fmt, cm, fuse, dt, seed):
         assert np.array_equal(s_gpu.view(np.uint32), s_ref.view(np.uint32))
     else:
         assert np.array_equal(s_gpu, s_ref)
+
+
+def _scaled_mode_cases(n=12, seed=777):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(n):
+        M = int(rng.choice([1, 17, 128, 129, 300, 1100, 2100]))
+        N = 8 * int(rng.integers(1, 300))
+        K = 128 * int(rng.integers(1, 20))
+        kind = ["ue8m0", "block_f32", "block_ue8m0"][i % 3]
+        pad = int(rng.choice([0, 16, 64]))
+        cases.append((M, N, K, kind, pad, bool(rng.integers(0, 2)), int(rng.integers(0, 2)), seed + i))
+    return cases
+
+
+@pytest.mark.parametrize("M,N,K,kind,pad,bias,out_dtype,seed", _scaled_mode_cases())
+def test_gemm_fuzz_packed_and_block_scales(M, N, K, kind, pad, bias, out_dtype, seed):
+    # packed UE8M0 group-128 A scales (as the quant writes them) and 128 x 128 block B
+    # scales, with a strided A
+    dev = require_gpu()
+    X = synth.to_bits(synth.normal((M, K), 1.0, seed=seed))
+    W = synth.to_bits(synth.normal((N, K), 0.02, seed=seed + 1))
+    if kind == "block_f32":
+        A, a_s, _ = oracle.group_quant_canonical(X, 0, 128)
+        a_fm, a_or, a_dev = fm.A_GROUP128, oracle.A_GROUP, to_dev(np.ascontiguousarray(a_s, np.float32), dev)
+    else:
+        A, a_s = oracle.group_quant(X, 0, 128, oracle.SCALE_UE8M0_PACKED, True)
+        a_fm, a_or, a_dev = fm.A_GROUP128_UE8M0, oracle.A_GROUP_UE8M0, to_dev(np.ascontiguousarray(a_s), dev)
+    if kind.startswith("block"):
+        B, b_s = oracle.quantize_blocks(W)
+        b_fm, b_or = fm.B_BLOCK128, oracle.B_BLOCK
+    else:
+        B, b_s = oracle.quantize_rows(W)
+        b_fm, b_or = fm.B_COL, oracle.B_COL
+    Aw = np.full((M, K + pad), 0x5A, np.uint8)
+    Aw[:, :K] = A
+    bias_bits = synth.to_bits(synth.normal((N,), 0.1, seed=seed + 2)) if bias else None
+    out = torch.empty((M, N), dtype=torch.bfloat16 if out_dtype == 0 else torch.float16, device=dev)
+    fm.fp8_scaled_mm(to_dev(Aw, dev), to_dev(B, dev), a_dev, to_dev(np.ascontiguousarray(b_s, np.float32), dev),
+                     a_fm | b_fm, out, bias=to_dev(bias_bits, dev).view(torch.bfloat16) if bias else None, K=K)
+    torch.cuda.synchronize()
+    assert fm.get_device_status() == 0
+    _, exact, sumabs = oracle.gemm(Aw, B, a_s, b_s, a_or, b_or, bias_bits=bias_bits, out_dtype=out_dtype, K=K,
+                                   want_exact=True)
+    check_gemm(bits(out), exact, sumabs, K, out_dtype, f"fuzz M{M} N{N} K{K} {kind} pad{pad}")
