@@ -359,6 +359,40 @@ def bench_group_quant(torch, fm, synth, dev, flush, reps=20):
     nbytes = rows * KM * 5 + rows * (KM // 512) * 4
     out["masked_silu_mul_ep_decode"] = {"us": round(us, 2), "bytes": nbytes, "gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
                                         "workload": f"E={E} T={T} K={KM}, {rows} token rows"}
+    # the same quant as a graph-captured decode runs it: 16 launches on distinct inputs
+    # replayed back to back from one CUDA graph (each a programmatic dependent of the one
+    # before), per-launch time
+    L = 16
+    xs = [synth.quant_input(E * T, 2 * KM, torch.bfloat16, seed=60 + i, device=dev).reshape(E, T, 2 * KM)
+          for i in range(L)]
+    qs = [torch.empty_like(qm) for _ in range(L)]
+    ss = [torch.empty_like(sm) for _ in range(L)]
+    st = torch.cuda.Stream()
+    st.wait_stream(torch.cuda.current_stream())
+
+    def chain(stream):
+        for i in range(L):
+            fm.silu_and_mul_masked_post_quant_fp8(xs[i], mm, qs[i], ss[i], 128, stream=stream)
+    with torch.cuda.stream(st):
+        chain(st)
+        st.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=st):
+            chain(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    tg = []
+    for _ in range(10):
+        flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        graph.replay()
+        b.record()
+        torch.cuda.synchronize()
+        tg.append(a.elapsed_time(b) * 1e3 / L)
+    ug = statistics.median(tg)
+    out["masked_silu_mul_ep_decode"]["graph_chain_16"] = {"us_per_launch": round(ug, 2),
+                                                          "gbs": round(nbytes / (ug * 1e-6) / 1e9, 1)}
+    del graph, xs, qs, ss
     return out
 
 
@@ -1023,6 +1057,9 @@ def main():
             "workload": f"M={QUANT_M} K={QUANT_K} bf16, group 128, UE8M0 packed column-major scales",
             "bound": "hbm", "peak_gbs": hbm_peak, "source_hash": qhash,
             **{k: dict(v, frac=round(v["gbs"] / hbm_peak, 4)) for k, v in gq.items()}}
+        gc = line["group_quant"]["masked_silu_mul_ep_decode"].get("graph_chain_16")
+        if gc:
+            gc["frac"] = round(gc["gbs"] / hbm_peak, 4)
         line["group_quant"]["plain"]["traffic"] = load_traffic("group_quant", qhash)
         line["group_quant"]["fused_silu_mul"]["traffic"] = load_traffic("group_quant", qhash,
                                                                         "fused_bytes_per_launch")
