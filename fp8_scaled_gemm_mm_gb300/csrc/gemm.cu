@@ -854,6 +854,64 @@ struct SplitArgs {
   int n_tiles;    // ceil(N / 128)
 };
 
+// The split-K reduction of the swap-AB kernel: thread t of the 128 epilogue threads
+// takes outputs idx = t, t + 128, ... of this rank's share (idx -> token m = idx /
+// quads, rows r_begin + 4 (idx % quads) .. + 3), sums the S partials of each in rank
+// order 0..S-1 through distributed shared memory, scales, adds the bias and stores.
+// U outputs per pass, all U x S loads issued before the first sum (S <= SMAX): with
+// two outputs a pass, large token blocks were bound by the remote-load round trips.
+struct SwapReduce {
+  uint32_t part_addr;
+  int t, total, quads, r_begin, S, m0, n0;
+  const float* vec_sa;
+  const float* vec_sb;
+  const float* vec_bias;
+
+  template <int U, int SMAX>
+  __device__ __forceinline__ void run(const GemmArgs& p, __nv_bfloat16* out) const {
+    for (int base = t; base < total; base += 128 * U) {
+      float4 pv[U][SMAX];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int idx = base + u * 128;
+        const int m = idx < total ? idx / quads : 0;
+        const int row = idx < total ? r_begin + 4 * (idx - m * quads) : r_begin;
+        const uint32_t off = static_cast<uint32_t>((m * 128 + row) * 4);
+#pragma unroll
+        for (int s2 = 0; s2 < SMAX; ++s2)
+          if (s2 < S && (U == 2 || idx < total))   // wide passes skip loads past the share
+            pv[u][s2] = ld_dsmem_f32x4(mapa_shared(part_addr + off, static_cast<uint32_t>(s2)));
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int idx = base + u * 128;
+        if (idx >= total) break;
+        float4 acc = pv[u][0];
+#pragma unroll
+        for (int s2 = 1; s2 < SMAX; ++s2) {
+          if (s2 < S) {
+            acc.x += pv[u][s2].x;
+            acc.y += pv[u][s2].y;
+            acc.z += pv[u][s2].z;
+            acc.w += pv[u][s2].w;
+          }
+        }
+        const int m = idx / quads;
+        const int row = r_begin + 4 * (idx - m * quads);
+        const int n = n0 + row;
+        if (n >= p.N) continue;
+        const float sa = vec_sa[m];
+        const float4 sb = *reinterpret_cast<const float4*>(vec_sb + row);
+        const float4 bs = *reinterpret_cast<const float4*>(vec_bias + row);
+        const float v0 = acc.x * sa * sb.x + bs.x, v1 = acc.y * sa * sb.y + bs.y;
+        const float v2 = acc.z * sa * sb.z + bs.z, v3 = acc.w * sa * sb.w + bs.w;
+        const int64_t o = static_cast<int64_t>(m0 + m) * p.N + n;
+        *reinterpret_cast<uint2*>(out + o) = make_uint2(pack2(v0, v1, p.out_fp16), pack2(v2, v3, p.out_fp16));
+      }
+    }
+  }
+};
+
 template <int BT>
 __global__ void __launch_bounds__(kThreads, 1)
     fp8_gemm_swap_splitk_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
@@ -1020,46 +1078,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool no_abort = true;
     for (int s2 = 0; s2 < S; ++s2)
       no_abort &= ld_dsmem_u32(mapa_shared(smem_u32(const_cast<int*>(abort_flag)), static_cast<uint32_t>(s2))) == 0;
-    // two outputs (x 4 rows) per thread per pass; all S partial loads of both are issued
-    // before any is summed (S <= 8), then summed in rank order
-    constexpr int U = 2;
-    for (int base = t; base < total && no_abort; base += 128 * U) {
-      float4 pv[U][8];
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int idx = base + u * 128;
-        const int m = idx < total ? idx / quads : 0;
-        const int row = idx < total ? r_begin + 4 * (idx - m * quads) : r_begin;
-        const uint32_t off = static_cast<uint32_t>((m * 128 + row) * 4);
-#pragma unroll
-        for (int s2 = 0; s2 < 8; ++s2)
-          if (s2 < S) pv[u][s2] = ld_dsmem_f32x4(mapa_shared(part_addr + off, static_cast<uint32_t>(s2)));
-      }
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int idx = base + u * 128;
-        if (idx >= total) break;
-        float4 acc = pv[u][0];
-#pragma unroll
-        for (int s2 = 1; s2 < 8; ++s2) {
-          if (s2 < S) {
-            acc.x += pv[u][s2].x;
-            acc.y += pv[u][s2].y;
-            acc.z += pv[u][s2].z;
-            acc.w += pv[u][s2].w;
-          }
-        }
-        const int m = idx / quads;
-        const int row = r_begin + 4 * (idx - m * quads);
-        const int n = n0 + row;
-        if (n >= p.N) continue;
-        const float sa = vec_sa[m];
-        const float4 sb = *reinterpret_cast<const float4*>(vec_sb + row);
-        const float4 bs = *reinterpret_cast<const float4*>(vec_bias + row);
-        const float v0 = acc.x * sa * sb.x + bs.x, v1 = acc.y * sa * sb.y + bs.y;
-        const float v2 = acc.z * sa * sb.z + bs.z, v3 = acc.w * sa * sb.w + bs.w;
-        const int64_t o = static_cast<int64_t>(m0 + m) * p.N + n;
-        *reinterpret_cast<uint2*>(out + o) = make_uint2(pack2(v0, v1, p.out_fp16), pack2(v2, v3, p.out_fp16));
+    // two outputs per thread per pass for 16- and 32-token blocks (decode: one pass);
+    // 64- and 128-token blocks keep about 16 remote loads in flight per thread
+    if (no_abort) {
+      const SwapReduce r{part_addr, t, total, quads, r_begin, S, m0, n0, vec_sa, vec_sb, vec_bias};
+      if constexpr (BT >= 64) {
+        if (S <= 2)
+          r.run<8, 2>(p, out);
+        else if (S <= 4)
+          r.run<4, 4>(p, out);
+        else
+          r.run<2, 8>(p, out);
+      } else {
+        r.run<2, 8>(p, out);
       }
     }
   }
