@@ -1418,14 +1418,15 @@ cudaError_t launch_swap(const CUtensorMap& tw, const CUtensorMap& tx, const Gemm
 // Split count for the small-M path: as many K slices (cluster size <= 8, at least two
 // K blocks each) as keep every CTA resident at two CTAs per SM, and no more than keep
 // the fp32 partials (S x token block x 128 x 4 bytes, written then read) under half
-// the weight bytes of a tile.
+// the weight bytes of a tile -- under all of them for 128-token blocks, whose CTAs
+// stream as many token bytes as weight bytes, so that more K slices shorten both
+// (measured at M = 128, K = 4096: four slices instead of two take N = 4096 from 18.8
+// to 16.5 us; 64-token blocks lose with eight slices instead of four).
 int pick_splits(int64_t M, int64_t N, int num_kb, int sms) {
   const int64_t tiles = static_cast<int64_t>(ceil_div(N, 128)) * ceil_div(M, 128);
   int s = 1;
-  // the partials written and read back grow with S x token block; keep them below
-  // half the weight slice a cluster streams
   const int64_t bt = M <= 16 ? 16 : (M <= 32 ? 32 : (M <= 64 ? 64 : 128));
-  const int64_t cap = static_cast<int64_t>(num_kb) * BK / (16 * bt);
+  const int64_t cap = static_cast<int64_t>(num_kb) * BK / ((bt == 128 ? 8 : 16) * bt);
   while (s < 8 && s + 1 <= cap && tiles * (s + 1) <= 2LL * sms && (s + 1) * 2 <= num_kb) ++s;
   return s;
 }

@@ -168,6 +168,14 @@ def test_small_m_boundaries(M):
     run_case(M, 1416, 2048, "row", "col", seed=M)
 
 
+@pytest.mark.parametrize("M,N,K", [(128, 1032, 4096), (97, 4096, 3072), (80, 1416, 2048)],
+                         ids=["4-way", "3-way", "2-way"])
+def test_small_m_wide_token_block_splits(M, N, K):
+    # 128-token blocks split K into up to four ranges; the reduction over them takes
+    # eight outputs per pass (two ranges) or four (three or four), ragged rows included
+    run_case(M, N, K, "row", "col", seed=M + K, bias=True)
+
+
 @pytest.mark.parametrize("K", [16, 48, 128, 400, 28672])
 def test_small_m_k_extremes(K):
     # K from a single partial K block to the largest K of the workloads
