@@ -84,10 +84,12 @@ def test_fused_silu_mul(dtype, fmt, colmajor, M, K):
 
 
 @pytest.mark.parametrize("dtype", [0, 1])
-@pytest.mark.parametrize("K", [512, 5376, 7168, 14336, 20480])
+@pytest.mark.parametrize("K", [512, 4096, 5376, 7168, 8192, 8208, 12288, 14336, 20480])
 @pytest.mark.parametrize("fuse", [False, True])
 def test_whole_row_group(dtype, K, fuse):
-    # one scale per row: rows held in registers (K <= 16384, unfused), or two passes
+    # one scale per row: rows held in registers (unfused; 128 threads a row with one to
+    # four 16-value segments each up to K = 8192, 256 threads with three or four up to
+    # 16384), or two passes
     x = synth.quant_input(33, 2 * K if fuse else K, DT[dtype], seed=41)
     for fmt, cm in ((0, False), (0, True), (2, True)):
         _compare(x, dtype, K, fmt, cm, fuse)
